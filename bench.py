@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-parallel layer forward on one B300 (per GPU).
+
+Headline: decode weight-stream GB/s on a Qwen2.5-1.5B-shaped stack -- 28
+serial pre-norm decoder layers (D=1536, SwiGLU F=8960, 12 Q / 2 KV heads of
+128), TP=2 logical shards, distinct random weights per layer (2.6 GB, far
+larger than the 126 MB L2, so no flush is needed) -- decoding one batch of
+each size in {1, 8, 32, 64} per step.  GB/s counts the unique projection
+weight bytes each forward must read (93,585,408 per layer).
+
+Alongside: prefill TFLOP/s of the Llama-3.1-70B-shaped MLP (X[4096, 8192],
+F=28672, TP=8), flops 2*B*D*2F + 2*B*F*D.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs an independent replica (weak scaling,
+no collective on the data path); value = units of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = "decode weight-stream GB/s & prefill TFLOP/s per TP-sharded layer, 1×B300"
+QW = si.QWEN_DECODE
+LP = si.LLAMA_PREFILL
+
+
+def layer_bytes(D, F, n_q, n_kv, hd):
+    return 2 * ((n_q + 2 * n_kv) * hd * D + D * n_q * hd + 3 * D * F)
+
+
+QWEN_LAYER_BYTES = layer_bytes(QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"])
+PREFILL_FLOPS = 2 * LP["B"] * LP["D"] * 2 * LP["F"] + 2 * LP["B"] * LP["F"] * LP["D"]
+
+
+def args_parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=QW["n_layers"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "samples": len(loaded), "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ------------------------------------------------------------- workloads
+
+def qwen_stack(n_layers, device):
+    return [si.layer_weights(QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], seed=0, layer=l,
+                             prefix="qwen", device=device) for l in range(n_layers)]
+
+
+def cpu_baseline(layers_dev, budget_s):
+    """The oracle, as it stands, on the host cores: one Qwen-shaped layer decoded
+    at each batch size, repeated until the budget is used; GB/s of weights."""
+    import numpy as np
+    from oracle import tp_layer as O
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([int(p.get("num_threads", 1)) for p in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        cores = len(os.sched_getaffinity(0))
+    W = {k: v.to("cpu", torch.float64).numpy() for k, v in layers_dev[0].items()}
+    xs = {B: si.activations(B, QW["D"], seed=1, name=f"bench.x{B}").to(torch.float64).numpy()
+          for B in QW["batches"]}
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for B in QW["batches"]:
+            O.decoder_layer(xs[B], W, QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"])
+            n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    del np
+    return {"value": n * QWEN_LAYER_BYTES / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n // len(QW['batches'])} passes of one Qwen-shaped TP=2 layer over B in "
+                      f"{list(QW['batches'])} (numpy float64), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle timed on the host cores, same metric and workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    from oracle import tp_layer as O
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = {k: v.to("cpu", torch.float64).numpy() for k, v in qwen_stack(1, dev)[0].items()}
+    xs = {B: si.activations(B, QW["D"], seed=1, name=f"bench.x{B}").to(torch.float64).numpy()
+          for B in QW["batches"]}
+
+    def step():
+        for B in QW["batches"]:
+            O.decoder_layer(xs[B], W, QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([int(p.get("num_threads", 1)) for p in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        cores = len(os.sched_getaffinity(0))
+    units = args.steps * len(QW["batches"]) * QWEN_LAYER_BYTES
+    value = units / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Qwen2.5-1.5B-shaped decode layer, TP=2 logical shards, B in {1,8,32,64} "
+                                   "(one layer per step: a bounded sample of the 28-layer stack)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps x one layer x 4 batches"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    del np
+    print(json.dumps(line), flush=True)
+
+
+def profile_pass(tpl, fn, stream):
+    """Per-launch device times of one call of fn: fn is captured into a CUDA
+    graph with the library's launch timing on (event-record nodes around every
+    kernel), replayed, and the last replay's times returned as [(tag, ms)]."""
+    tpl.profile_enable(8192)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    rec = tpl.profile_records()
+    tpl.profile_disable()
+    del g
+    return rec
+
+
+def main():
+    args = args_parse()
+    rank, world = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import mlp_megatron_tp_layer_b300 as tpl
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_kind = measured_peaks()
+    D, F, n_q, n_kv, hd, tp = QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"]
+    batches = QW["batches"]
+    L = args.layers
+
+    layers = qwen_stack(L, dev)
+    xs = {B: si.activations(B, D, seed=1, name=f"bench.x{B}", device=dev) for B in batches}
+    ys = {B: torch.empty_like(xs[B]) for B in batches}
+    ws = tpl.workspace(max(tpl.decoder_workspace_bytes(B, D, F, n_q, n_kv, hd, tp) for B in batches), dev)
+
+    def forward(B, x=None, y=None):
+        tpl.tp_decoder_stack(xs[B] if x is None else x, layers, n_q, n_kv, hd, tp,
+                             out=ys[B] if y is None else y, ws=ws)
+
+    def eager_step():
+        for B in batches:
+            forward(B)
+
+    # launch list and per-kernel device times (inside a graph, events around each launch)
+    stream = torch.cuda.Stream(device=dev)
+    eager_step()
+    torch.cuda.synchronize()
+    recs = profile_pass(tpl, eager_step, stream)
+    # launch_rmsnorm scopes also hold two small zeroing kernels
+    launches_per_step = len(recs) + 2 * sum(1 for t, _ in recs if t == "rmsnorm")
+
+    # CUDA graphs: one per batch size, replaying the library's launches
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for B in batches:
+            forward(B)
+    torch.cuda.synchronize()
+    for B in batches:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            forward(B)
+        graphs[B] = g
+    torch.cuda.synchronize()
+
+    def step():
+        for B in batches:
+            graphs[B].replay()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, world)
+    units_per_step = L * len(batches) * QWEN_LAYER_BYTES
+    value = units_per_step * args.steps * world / (ms / 1e3) / 1e9
+
+    # per-batch breakdown
+    per_batch = {}
+    for B in batches:
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(max(3, args.steps // 2)):
+            graphs[B].replay()
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / max(3, args.steps // 2)
+        per_batch[str(B)] = {"ms_per_forward": t, "GB/s": L * QWEN_LAYER_BYTES / (t / 1e3) / 1e9,
+                             "TFLOP/s": 2 * B * L * QWEN_LAYER_BYTES / 2 / (t / 1e3) / 1e12}
+
+    # end to end: pinned host x in, host y out, inside the timed region
+    hx = {B: xs[B].to("cpu").pin_memory() for B in batches}
+    hy = {B: torch.empty_like(hx[B]).pin_memory() for B in batches}
+    with torch.cuda.stream(stream):
+        for B in batches:
+            xs[B].copy_(hx[B], non_blocking=True)
+    torch.cuda.synchronize()
+    h2d = sum(hx[B].numel() * hx[B].element_size() for B in batches)
+    d2h = sum(hy[B].numel() * hy[B].element_size() for B in batches)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            for B in batches:
+                xs[B].copy_(hx[B], non_blocking=True)
+                graphs[B].replay()
+                hy[B].copy_(ys[B], non_blocking=True)
+            stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": units_per_step * args.steps * world / e2e_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # roofline of the dominant kernel (largest total device time in the launch list)
+    tot = {}
+    for tag, t in recs:
+        n, s = tot.get(tag, (0, 0.0))
+        tot[tag] = (n + 1, s + t)
+    dom = max(tot, key=lambda k: tot[k][1])
+    alg = {"gateup": lambda B: 2 * F * D * 2 + B * D * 2 + B * F * 2,
+           "down": lambda B: D * F * 2 + B * F * 2 + B * D * 4 * 0,
+           "qkv": lambda B: (n_q + 2 * n_kv) * hd * D * 2 + B * D * 2,
+           "oproj": lambda B: D * n_q * hd * 2 + B * n_q * hd * 2}
+    roof = None
+    if dom in alg:
+        per_b = L  # launches of one tag per forward
+        total_bytes = 0
+        for B in batches:
+            total_bytes += alg[dom](B) * per_b
+        n_launch, t_ms = tot[dom]
+        achieved = total_bytes / (t_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                "launches": n_launch, "avg_launch_us": t_ms / n_launch * 1e3,
+                "algorithmic_bytes_per_launch_avg": total_bytes / n_launch}
+    share = {k: {"launches": v[0], "ms": v[1], "share": v[1] / sum(x[1] for x in tot.values())}
+             for k, v in sorted(tot.items(), key=lambda kv: -kv[1][1])}
+    # per batch size: average device time of each step of one layer (us)
+    per_fwd = len(recs) // len(batches)
+    for bi, B in enumerate(batches):
+        grp = recs[bi * per_fwd:(bi + 1) * per_fwd]
+        agg = {}
+        for tag, t in grp:
+            n, s_ = agg.get(tag, (0, 0.0))
+            agg[tag] = (n + 1, s_ + t)
+        per_batch[str(B)]["kernel_us"] = {k: round(v[1] / v[0] * 1e3, 2) for k, v in agg.items()}
+        per_batch[str(B)]["sum_kernel_us_per_layer"] = round(sum(v[1] for v in agg.values()) / L * 1e3, 2)
+
+    # prefill MLP (Llama-3.1-70B-shaped, TP=8)
+    prefill = None
+    if not args.no_prefill:
+        P = si.prefill_mlp(LP["B"], LP["D"], LP["F"], seed=0, device=dev)
+        Yp = torch.empty((LP["B"], LP["D"]), dtype=torch.bfloat16, device=dev)
+        pws = tpl.workspace(tpl.mlp_workspace_bytes(LP["B"], LP["D"], LP["F"], LP["tp"]), dev)
+
+        def pstep():
+            tpl.tp_mlp_forward(P["X"], P["Wg"], P["Wu"], P["Wd"], LP["tp"], out=Yp, ws=pws)
+
+        for _ in range(max(3, args.warmup)):
+            pstep()
+        precs = profile_pass(tpl, pstep, stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        psteps = max(5, args.steps // 5)
+        a.record()
+        for _ in range(psteps):
+            pstep()
+        b.record()
+        torch.cuda.synchronize()
+        pms = max_over_ranks(a.elapsed_time(b) / psteps, world)
+        gu = [t for tag, t in precs if tag == "gateup"]
+        dn = [t for tag, t in precs if tag == "down"]
+        gu_flops = 2 * LP["B"] * LP["D"] * 2 * LP["F"]
+        dn_flops = 2 * LP["B"] * LP["F"] * LP["D"]
+        prefill = {"workload": "Llama-3.1-70B-shaped prefill MLP X[4096,8192], F=28672, TP=8, fused shard reduce",
+                   "value": PREFILL_FLOPS / (pms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": pms,
+                   "roofline": {"bound": "tensor", "kernel": "gateup", "achieved": gu_flops / (gu[0] / 1e3) / 1e12,
+                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": gu_flops / (gu[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
+                                "traffic": None, "peak_kind": peak_kind + " burst"} if gu else None,
+                   "down_TFLOP/s": dn_flops / (dn[0] / 1e3) / 1e12 if dn else None,
+                   "launches_per_step": len(precs)}
+        del P
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"Qwen2.5-1.5B-shaped decode: {L} serial pre-norm layers D=1536 F=8960 "
+                                       f"12Q/2KV heads x128, TP=2 logical shards, one forward per B in "
+                                       f"{list(batches)} per step",
+                           "global_batch": sum(batches), "parallelism": "tp2 logical shards; 1 replica per GPU",
+                           "l2": f"weights {L * QWEN_LAYER_BYTES / 1e9:.2f} GB per forward > 126 MB L2; no flush",
+                           "graphs": "one CUDA graph per batch size"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+                "per_batch": per_batch, "kernel_share": share, "prefill": prefill}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * tpl.h -- Megatron-style tensor-parallel layer forward on one GPU (C ABI).
+ *
+ * The tensor-parallel (TP) shards are logical partitions of the weights held
+ * in one GPU's memory.  What would be a cross-device all-reduce of per-shard
+ * partial sums becomes an on-device partial-sum reduction.
+ *
+ * Sources (reference pages, by title and section):
+ *   [L4] "Lecture 4 - Distributed Serving" (CS349E notes): S3.1 sharding
+ *        notation A[I_X, J]; S3.2 the four sharded-matmul cases; S4.1 MLP
+ *        column-then-row split; S4.2 attention split by head; S4.3 the
+ *        sharded output equals the single-device output up to summation
+ *        order; S4.4 KV groups when tp > n_kv.
+ *   [V4] "vLLM model parallelism" article: S2.1 ColumnParallelLinear keeps its
+ *        weight as [output_size_per_partition, input_size] and applies
+ *        F.linear; RowParallelLinear splits along the input and all-reduces.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensor pointers are DEVICE pointers into the calling process's current
+ *    CUDA device.  The caller owns all memory; the library keeps no pointer
+ *    after a call returns and never allocates device memory on these paths.
+ *  - Matrices are row-major.  Weights are stored [out, in] (the nn.Linear /
+ *    [V4] layout): y = x W^T.  A dimension split over tp shards is split in
+ *    tp contiguous blocks; shard s holds block s ([L4] S3.1).
+ *  - A tensor sharded along its LAST dimension, e.g. C[I, K_X], is stored as
+ *    the concatenation of the shard-local pieces: [X, I, K/X].  One sharded
+ *    along its first dimension, C[I_X, K], is [I, K] row-major.
+ *  - dtype TPL_BF16: activations and weights are bfloat16; products
+ *    accumulate in fp32; partial sums are fp32; intermediates the next
+ *    product consumes (SwiGLU output, packed QKV, attention output) are
+ *    rounded to bf16.  The final output has element type out_dtype: TPL_BF16
+ *    (rounded to nearest even) or TPL_F32 (the unrounded fp32 result).
+ *    dtype TPL_F32: everything fp32 (CUDA-core fp32 FMA, no TF32); out_dtype
+ *    must then be TPL_F32.
+ *  - Every pointer must be 16-byte aligned and every row length (in bytes) a
+ *    multiple of 16; otherwise TPL_ERR_ALIGN.  Outputs must not overlap
+ *    inputs (TPL_ERR_ALIAS).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work; they are asynchronous and
+ *    stream-ordered.  Arguments are validated before anything is launched: a
+ *    call that returns an error has launched nothing.  Launch failures return
+ *    TPL_ERR_CUDA.  Faults during execution surface at the caller's next
+ *    synchronisation, like any CUDA kernel.
+ *  - Kernels never spin without bound.  A device-side wait that gives up sets
+ *    a sticky device error word, read and cleared with tpl_device_status().
+ *  - `ws` is caller-provided scratch of at least the size the matching
+ *    *_workspace() query returns (TPL_ERR_WORKSPACE otherwise).  Its contents
+ *    on entry do not matter; calls sharing one `ws` must be stream-ordered.
+ */
+#ifndef TPL_H
+#define TPL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tpl_status {
+    TPL_OK = 0,
+    TPL_ERR_NULL = 1,         /* a required pointer is NULL                        */
+    TPL_ERR_SHAPE = 2,        /* size <= 0, or not divisible by the shard count     */
+    TPL_ERR_ALIGN = 3,        /* pointer or row pitch not a multiple of 16 bytes    */
+    TPL_ERR_DTYPE = 4,        /* dtype not supported by this call                   */
+    TPL_ERR_WORKSPACE = 5,    /* ws NULL or smaller than the workspace query        */
+    TPL_ERR_UNSUPPORTED = 6,  /* argument combination not supported (see the call)  */
+    TPL_ERR_CUDA = 7,         /* the CUDA runtime reported an error                 */
+    TPL_ERR_TIMEOUT = 8,      /* a device-side bounded wait gave up                 */
+    TPL_ERR_ALIAS = 9         /* an output buffer overlaps an input buffer          */
+} tpl_status;
+
+typedef enum tpl_dtype { TPL_F32 = 0, TPL_BF16 = 1 } tpl_dtype;
+
+/* How a partial-sum reduction distributes its result ([L4] S3.2 case 3):
+ * ALLREDUCE: every shard holds the full sum -> one [rows, cols] copy here.
+ * REDUCE_SCATTER: shard s keeps columns [s cols/tp, (s+1) cols/tp), stored
+ * shard-blocked as [tp, rows, cols/tp]. */
+typedef enum tpl_reduce_mode { TPL_ALLREDUCE = 0, TPL_REDUCE_SCATTER = 1 } tpl_reduce_mode;
+
+/* Case 4 of [L4] S3.2 needs one operand all-gathered first. */
+typedef enum tpl_gather { TPL_GATHER_B = 0, TPL_GATHER_A = 1 } tpl_gather;
+
+/* Device error word bits (tpl_device_status). */
+#define TPL_DEVERR_TIMEOUT 0x1u   /* an mbarrier wait exceeded its time limit */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* tpl_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int tpl_version(void);
+
+/* Reads and clears the sticky device error word after synchronising `stream`.
+ * *flags receives TPL_DEVERR_* bits (0 = no device-side error). */
+tpl_status tpl_device_status(unsigned int* flags, void* stream);
+
+/* --------------------------------------------------------------------------
+ * shard_reduce -- the all-reduce stand-in ([L4] S3.2 case 3, S4.1, S4.2).
+ *
+ * out = partials[0] + partials[1] + ... + partials[tp-1], added left to right
+ * in fp32, for a [rows, cols] result.
+ *   partials : fp32 [tp, rows, cols], shard-major.               (input)
+ *   out      : [rows, cols] (ALLREDUCE) or [tp, rows, cols/tp]
+ *              (REDUCE_SCATTER), element type out_dtype.          (output)
+ *   tp >= 1; REDUCE_SCATTER needs cols % tp == 0.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_shard_reduce(const float* partials, void* out, int64_t rows, int64_t cols,
+                            int tp, int mode, int out_dtype, void* stream);
+
+/* --------------------------------------------------------------------------
+ * tp_mlp_forward -- Megatron SwiGLU MLP, column then row ([L4] S4.1).
+ *
+ *   X  [B, D]            input tokens (replicated on every shard).
+ *   Wg, Wu [F, D]        gate / up weights; shard s uses rows
+ *                        [s F/tp, (s+1) F/tp) (column-parallel, case 1).
+ *   Wd [D, F]            down weight; shard s uses columns
+ *                        [s F/tp, (s+1) F/tp) (row-parallel, case 3).
+ *   Y  [B, D]            output, sum over shards of H_s Wd_s^T.
+ *   partials             optional fp32 [tp, B, D]: if non-NULL the per-shard
+ *                        partials P_s = H_s Wd_s^T are written there and then
+ *                        reduced by the shard_reduce kernel; if NULL the
+ *                        reduction is fused into the down projection
+ *                        (shard partials accumulated in ascending s order).
+ * H_s = silu(X Wg_s^T) * (X Wu_s^T) with silu(z) = z / (1 + exp(-z)); for
+ * TPL_BF16 H is rounded to bf16 (it is the down projection's operand).
+ * F % tp == 0 and D % 8 == 0, F % 8 == 0 are required (TPL_ERR_SHAPE / ALIGN).
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_tp_mlp_forward_workspace(int64_t B, int64_t D, int64_t F, int tp, int dtype,
+                                        size_t* bytes);
+tpl_status tpl_tp_mlp_forward(const void* X, const void* Wg, const void* Wu, const void* Wd,
+                              void* Y, float* partials, int64_t B, int64_t D, int64_t F, int tp,
+                              int dtype, int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * tp_attn_proj -- attention projections split by head ([L4] S4.2, S4.4).
+ *
+ *   X     [B, D]
+ *   Wqkv  [(n_q + 2 n_kv) head_dim, D], rows [Q heads | K heads | V heads],
+ *         each head head_dim consecutive rows.
+ *   Wo    [D, n_q head_dim]; shard s uses the columns of its Q heads.
+ *   qkv_out optional: per shard s, [B, (nq_s + 2 nkv_s) head_dim] in
+ *         [Q_s | K_s | V_s] order, shards concatenated ([tp, B, ...]).
+ *   Y     [B, D] = sum over shards of O_s Wo_s^T.
+ *   partials optional fp32 [tp, B, D] as in tp_mlp_forward.
+ * Shard s owns Q heads [s n_q/tp, (s+1) n_q/tp).  If tp <= n_kv it owns KV
+ * groups [s n_kv/tp, (s+1) n_kv/tp) (needs n_kv % tp == 0); if tp > n_kv it
+ * holds a copy of KV group floor(s n_kv / tp) (needs tp % n_kv == 0).
+ * The attention core between the projections is not part of this library:
+ * O_s is the attention output for a context of one token (the token itself),
+ * where softmax over one key is exactly 1, so Q head h outputs the value
+ * vector of its KV group floor(h n_kv / n_q).
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_tp_attn_proj_workspace(int64_t B, int64_t D, int n_q, int n_kv, int head_dim,
+                                      int tp, int dtype, size_t* bytes);
+tpl_status tpl_tp_attn_proj(const void* X, const void* Wqkv, const void* Wo, void* qkv_out,
+                            void* Y, float* partials, int64_t B, int64_t D, int n_q, int n_kv,
+                            int head_dim, int tp, int dtype, int out_dtype, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * sharded_matmul -- C = A B in one of the four cases of [L4] S3.2, over X
+ * logical devices.  A [I, J] row-major; B [J, K] stored transposed as
+ * Bt [K, J] (the [out, in] weight layout).
+ *   case 1: A[I_X, J] B[J, K]   -> C[I_X, K] stored [I, K]; no communication.
+ *   case 2: A[I, J_X] B[J, K]   -> all-gather A (a view here), C[I, K].
+ *   case 3: A[I, J_X] B[J_X, K] -> partial sums over J blocks, then
+ *           mode ALLREDUCE: C[I, K]; REDUCE_SCATTER: C[I, K_X] ([X, I, K/X]).
+ *           partials optional fp32 [X, I, K] as in tp_mlp_forward.
+ *   case 4: A[I_X, J] B[J, K_X] -> gather TPL_GATHER_B: case 1, C[I, K];
+ *           TPL_GATHER_A: C[I, K_X] stored [X, I, K/X].
+ * The sharded dimensions must divide by X (TPL_ERR_SHAPE).
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_sharded_matmul_workspace(int case_id, int mode, int64_t I, int64_t J, int64_t K,
+                                        int X, int dtype, size_t* bytes);
+tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, const void* A, const void* Bt,
+                              void* C, float* partials, int64_t I, int64_t J, int64_t K, int X,
+                              int dtype, int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * tp_decoder_layer / tp_decoder_stack -- serial pre-norm decoder layer built
+ * from the calls above (bf16 only):
+ *   h = x + Attn(RMSNorm(x));  y = h + MLP(RMSNorm(h))
+ * RMSNorm has unit gain and eps = 1e-6 and is computed on every shard
+ * ([L4] S4.2: replicated).  Attn and MLP are tp_attn_proj and tp_mlp_forward
+ * with the shard reduction fused with the residual add.  x, y [B, D] bf16;
+ * y may equal x.  The stack applies n_layers layers in order; the weight
+ * pointer arrays live in HOST memory, one device pointer per layer.
+ * This composition goes beyond the pages' four operations; it exists to run
+ * a whole decode step.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_tp_decoder_workspace(int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
+                                    int head_dim, int tp, size_t* bytes);
+tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* Wqkv, const void* Wo,
+                                const void* Wg, const void* Wu, const void* Wd, int64_t B,
+                                int64_t D, int64_t F, int n_q, int n_kv, int head_dim, int tp,
+                                void* ws, size_t ws_bytes, void* stream);
+tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv,
+                                const void* const* Wo, const void* const* Wg,
+                                const void* const* Wu, const void* const* Wd, int n_layers,
+                                int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int head_dim,
+                                int tp, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * Launch timing, for measurement only (off by default).
+ * tpl_profile_enable(n > 0) creates n pairs of CUDA events (host objects; no
+ * device memory) and from then on brackets each kernel launch with a pair on
+ * the launch's stream, tagged with the step it implements ("qkv", "oproj",
+ * "gateup", "down", "matmul", "reduce", "reduce_norm", "rmsnorm").  Launches
+ * beyond n are not recorded.  tpl_profile_enable(0) turns it off and frees the
+ * events.  tpl_profile_count() is the number of recorded launches;
+ * tpl_profile_read(i, ...) waits for launch i and returns its tag and its
+ * device time in milliseconds.  Under CUDA-graph capture the event records
+ * become nodes of the graph; the times read are those of its latest replay.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_profile_enable(int max_launches);
+int tpl_profile_count(void);
+tpl_status tpl_profile_read(int i, char* tag, size_t tag_len, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPL_H */

@@ -1,0 +1,336 @@
+"""Megatron tensor-parallel layer forward on one B300: Python binding.
+
+Thin ctypes binding of ``libtpl.so`` (declared in ``include/tpl.h``): it only
+checks and marshals arguments (pointers, sizes, the current CUDA stream); every
+step of the computation runs in the library's CUDA kernels.  PyTorch supplies
+device memory and streams.
+
+The library must be built (``python mlp_megatron_tp_layer_b300/build.py``);
+importing this package without it raises ImportError -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtpl.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "tpl.h")
+
+F32, BF16 = 0, 1
+ALLREDUCE, REDUCE_SCATTER = 0, 1
+GATHER_B, GATHER_A = 0, 1
+STATUS = {0: "TPL_OK", 1: "TPL_ERR_NULL", 2: "TPL_ERR_SHAPE", 3: "TPL_ERR_ALIGN", 4: "TPL_ERR_DTYPE",
+          5: "TPL_ERR_WORKSPACE", 6: "TPL_ERR_UNSUPPORTED", 7: "TPL_ERR_CUDA", 8: "TPL_ERR_TIMEOUT",
+          9: "TPL_ERR_ALIAS"}
+
+_vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "tpl_status_string": (ctypes.c_char_p, [_i32]),
+    "tpl_version": (_i32, []),
+    "tpl_device_status": (_i32, [ctypes.POINTER(ctypes.c_uint), _vp]),
+    "tpl_shard_reduce": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
+    "tpl_tp_mlp_forward_workspace": (_i32, [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tpl_tp_mlp_forward": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
+                                  _vp, _sz, _vp]),
+    "tpl_tp_attn_proj_workspace": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tpl_tp_attn_proj": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
+                                _i32, _vp, _sz, _vp]),
+    "tpl_sharded_matmul_workspace": (_i32, [_i32, _i32, _i64, _i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tpl_sharded_matmul": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
+                                  _vp, _sz, _vp]),
+    "tpl_profile_enable": (_i32, [_i32]),
+    "tpl_profile_count": (_i32, []),
+    "tpl_profile_read": (_i32, [_i32, ctypes.c_char_p, _sz, ctypes.POINTER(ctypes.c_float)]),
+    "tpl_tp_decoder_workspace": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tpl_tp_decoder_layer": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
+                                    _i32, _vp, _sz, _vp]),
+    "tpl_tp_decoder_stack": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                    ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
+                                    _i32, _i32, _i32, _vp, _sz, _vp]),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python mlp_megatron_tp_layer_b300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tpl.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\*|tpl_status|int)\s+(tpl_\w+)\s*\(", text, re.M)))
+
+
+class TplError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = lib.tpl_status_string(status).decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({msg})")
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise TplError(status, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _tdt(code: int):
+    return torch.bfloat16 if code == BF16 else torch.float32
+
+
+def _out_code(dt: int, out, out_dtype) -> int:
+    """Output element type: the given out tensor's, else out_dtype, else the input's."""
+    if out is not None:
+        code = _dt(out)
+        if out_dtype is not None and _dt(torch.empty(0, dtype=out_dtype)) != code:
+            raise ValueError("out and out_dtype disagree")
+        return code
+    return dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (row-major)")
+
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A cached scratch buffer of at least nbytes on device (grown on demand)."""
+    dev = torch.device(device)
+    key = (dev.type, dev.index)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _ws_cache[key] = buf
+    return buf
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device error word."""
+    flags = ctypes.c_uint(0)
+    st = lib.tpl_device_status(ctypes.byref(flags), _stream(stream))
+    if st not in (0, 8):
+        raise TplError(st, "tpl_device_status")
+    return flags.value
+
+
+# ------------------------------------------------------------------- calls
+
+def shard_reduce(partials: torch.Tensor, mode: int = ALLREDUCE, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Sum fp32 partials [tp, rows, cols] over shards in ascending order."""
+    _contig(partials)
+    tp, rows, cols = partials.shape
+    if out is None:
+        shape = (rows, cols) if mode == ALLREDUCE else (tp, rows, cols // tp)
+        out = torch.empty(shape, dtype=out_dtype, device=partials.device)
+    _contig(out)
+    _check(lib.tpl_shard_reduce(_p(partials), _p(out), rows, cols, tp, mode, _dt(out), _stream(stream)),
+           "tpl_shard_reduce")
+    return out
+
+
+def mlp_workspace_bytes(B, D, F, tp, dtype=BF16) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_tp_mlp_forward_workspace(B, D, F, tp, dtype, ctypes.byref(n)), "tpl_tp_mlp_forward_workspace")
+    return n.value
+
+
+def tp_mlp_forward(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=None, ws=None, stream=None):
+    """Y = sum_s (silu(X Wg_s^T) * (X Wu_s^T)) Wd_s^T over tp logical shards.
+
+    ``partials``: None (reduction fused), True (allocate) or an fp32 [tp, B, D] tensor.
+    Returns Y, or (Y, partials) when partials were requested.
+    """
+    _contig(X, Wg, Wu, Wd)
+    B, D = X.shape
+    F = Wg.shape[0]
+    dt = _dt(X)
+    odt = _out_code(dt, out, out_dtype)
+    if out is None:
+        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
+    want = partials is not None and partials is not False
+    if partials is True:
+        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
+    elif not want:
+        partials = None
+    nbytes = mlp_workspace_bytes(B, D, F, tp, dt)
+    ws = workspace(nbytes, X.device) if ws is None else ws
+    _check(lib.tpl_tp_mlp_forward(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp, dt, odt,
+                                  _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "tpl_tp_mlp_forward")
+    return (out, partials) if want else out
+
+
+def attn_workspace_bytes(B, D, n_q, n_kv, head_dim, tp, dtype=BF16) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_tp_attn_proj_workspace(B, D, n_q, n_kv, head_dim, tp, dtype, ctypes.byref(n)),
+           "tpl_tp_attn_proj_workspace")
+    return n.value
+
+
+def qkv_shard_width(n_q, n_kv, head_dim, tp) -> int:
+    kv_s = n_kv // tp if tp <= n_kv else 1
+    return (n_q // tp + 2 * kv_s) * head_dim
+
+
+def tp_attn_proj(X, Wqkv, Wo, n_q, n_kv, head_dim, tp, out=None, qkv_out=None, partials=None, out_dtype=None,
+                 ws=None, stream=None):
+    """Head-partitioned QKV projection, context-1 attention stand-in, row-parallel o_proj.
+
+    ``qkv_out``: None, True (allocate [tp, B, W_s]) or a tensor.  ``partials`` as in
+    tp_mlp_forward.  Returns Y, plus qkv_out / partials when requested (in that order).
+    """
+    _contig(X, Wqkv, Wo)
+    B, D = X.shape
+    dt = _dt(X)
+    odt = _out_code(dt, out, out_dtype)
+    if out is None:
+        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
+    want_qkv = qkv_out is not None and qkv_out is not False
+    if qkv_out is True:
+        qkv_out = torch.empty((tp, B, qkv_shard_width(n_q, n_kv, head_dim, tp)), dtype=X.dtype, device=X.device)
+    elif not want_qkv:
+        qkv_out = None
+    want_p = partials is not None and partials is not False
+    if partials is True:
+        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
+    elif not want_p:
+        partials = None
+    nbytes = attn_workspace_bytes(B, D, n_q, n_kv, head_dim, tp, dt)
+    ws = workspace(nbytes, X.device) if ws is None else ws
+    _check(lib.tpl_tp_attn_proj(_p(X), _p(Wqkv), _p(Wo), _p(qkv_out), _p(out), _p(partials), B, D, n_q, n_kv,
+                                head_dim, tp, dt, odt, _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpl_tp_attn_proj")
+    res = [out]
+    if want_qkv:
+        res.append(qkv_out)
+    if want_p:
+        res.append(partials)
+    return res[0] if len(res) == 1 else tuple(res)
+
+
+def case_workspace_bytes(case, mode, I, J, K, X, dtype=BF16) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_sharded_matmul_workspace(case, mode, I, J, K, X, dtype, ctypes.byref(n)),
+           "tpl_sharded_matmul_workspace")
+    return n.value
+
+
+def sharded_matmul(case: int, A, Bt, X: int, mode: int = ALLREDUCE, gather: int = GATHER_B, out=None,
+                   partials=None, out_dtype=None, ws=None, stream=None):
+    """C = A B (B stored as Bt[K, J]) in one of the four sharding cases over X devices.
+
+    K-sharded results (case 3 reduce-scatter, case 4 gather-A) are [X, I, K/X].
+    """
+    _contig(A, Bt)
+    I, J = A.shape
+    K = Bt.shape[0]
+    dt = _dt(A)
+    odt = _out_code(dt, out, out_dtype)
+    k_sharded = (case == 3 and mode == REDUCE_SCATTER) or (case == 4 and gather == GATHER_A)
+    if out is None:
+        shape = (X, I, K // X) if k_sharded else (I, K)
+        out = torch.empty(shape, dtype=_tdt(odt), device=A.device)
+    want_p = partials is not None and partials is not False
+    if partials is True:
+        partials = torch.empty((X, I, K), dtype=torch.float32, device=A.device)
+    elif not want_p:
+        partials = None
+    nbytes = case_workspace_bytes(case, mode, I, J, K, X, dt)
+    ws = workspace(nbytes, A.device) if ws is None else ws
+    _check(lib.tpl_sharded_matmul(case, mode, gather, _p(A), _p(Bt), _p(out), _p(partials), I, J, K, X, dt, odt,
+                                  _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "tpl_sharded_matmul")
+    return (out, partials) if want_p else out
+
+
+def decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_tp_decoder_workspace(B, D, F, n_q, n_kv, head_dim, tp, ctypes.byref(n)),
+           "tpl_tp_decoder_workspace")
+    return n.value
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return arr
+
+
+def tp_decoder_stack(x, layers, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=None):
+    """Serial pre-norm decoder layers; ``layers`` is a list of dicts with Wqkv, Wo, Wg, Wu, Wd."""
+    _contig(x)
+    B, D = x.shape
+    F = layers[0]["Wg"].shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    nbytes = decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp)
+    ws = workspace(nbytes, x.device) if ws is None else ws
+    arrs = [_ptr_array([L[k] for L in layers]) for k in ("Wqkv", "Wo", "Wg", "Wu", "Wd")]
+    _check(lib.tpl_tp_decoder_stack(_p(x), _p(out), *arrs, len(layers), B, D, F, n_q, n_kv, head_dim, tp, _p(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "tpl_tp_decoder_stack")
+    return out
+
+
+def tp_decoder_layer(x, W, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=None):
+    """One serial pre-norm decoder layer (see tp_decoder_stack)."""
+    _contig(x)
+    B, D = x.shape
+    F = W["Wg"].shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    nbytes = decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp)
+    ws = workspace(nbytes, x.device) if ws is None else ws
+    _check(lib.tpl_tp_decoder_layer(_p(x), _p(out), _p(W["Wqkv"]), _p(W["Wo"]), _p(W["Wg"]), _p(W["Wu"]),
+                                    _p(W["Wd"]), B, D, F, n_q, n_kv, head_dim, tp, _p(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "tpl_tp_decoder_layer")
+    return out
+
+
+def profile_enable(max_launches: int = 4096):
+    """Start recording per-launch device times (see tpl_profile_enable)."""
+    _check(lib.tpl_profile_enable(max_launches), "tpl_profile_enable")
+
+
+def profile_disable():
+    _check(lib.tpl_profile_enable(0), "tpl_profile_enable")
+
+
+def profile_records():
+    """[(tag, ms)] for every launch recorded since profile_enable."""
+    out = []
+    buf = ctypes.create_string_buffer(64)
+    ms = ctypes.c_float(0.0)
+    for i in range(lib.tpl_profile_count()):
+        _check(lib.tpl_profile_read(i, buf, 64, ctypes.byref(ms)), "tpl_profile_read")
+        out.append((buf.value.decode(), float(ms.value)))
+    return out

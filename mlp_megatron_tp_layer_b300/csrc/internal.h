@@ -1,0 +1,126 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/tpl.h"
+
+namespace tpl {
+
+// ---------------------------------------------------------------- epilogues
+// How a GEMM-like kernel writes the value v computed for (token t, feature f).
+// "token" is the row of the activation operand, "feature" the row of the
+// [out, in] weight (the output column).
+enum EpiMode : int {
+    EPI_STORE = 0,    // out[t*ldo + f] (optionally column-blocked), dtype of the call
+    EPI_PARTIAL = 1,  // fp32 out32[split*split_stride + t*ldo + f]
+    EPI_SWIGLU = 2,   // out[t*ldo + f] = silu(gate) * up   (needs full sums)
+    EPI_QKV = 3,      // scatter packed-QKV row f to each shard block, V rows also to O
+    EPI_PARTIAL2 = 4  // two fp32 partial planes (gate, up) for split SwiGLU
+};
+
+struct QkvMap {
+    int n_q, n_kv, head_dim, tp;
+    int nq_s, kv_s;        // Q heads / KV groups held by one shard
+    int64_t shard_stride;  // elements between shard blocks of qkv_out ([tp, B, W_s])
+    int64_t w_s;           // row length of one shard block: (nq_s + 2 kv_s) * head_dim
+    void* qkv_out;         // [tp, B, w_s]
+    void* o_out;           // [B, n_q * head_dim] attention stand-in output
+    int64_t ldo_o;
+};
+
+struct Epilogue {
+    int mode;
+    int out_bf16;          // output element type for EPI_STORE / EPI_SWIGLU (1 = bf16, 0 = fp32)
+    void* out;             // EPI_STORE, EPI_SWIGLU
+    float* out32;          // EPI_PARTIAL / EPI_PARTIAL2 (plane 0)
+    float* out32b;         // EPI_PARTIAL2 plane 1
+    int64_t ldo;           // row pitch of the output in elements
+    int64_t col_block;     // > 0: output column f lives at (f / col_block) * block_stride + f % col_block
+    int64_t block_stride;
+    int64_t split_stride;  // EPI_PARTIAL(2): elements between split planes
+    QkvMap qkv;
+    unsigned int* zero_words;  // if set, block 0 of the launch zeroes zero_count words at start
+    int zero_count;            // (row accumulators of the reduction that consumes this output)
+};
+
+// Work split of the contracting dimension: K = tp shards of k_shard elements,
+// each shard cut into `sub` chunks of k_chunk elements (the last may be shorter).
+// Split index = shard * sub + j.
+struct KSplit {
+    int64_t k_shard;
+    int64_t k_chunk;
+    int tp;
+    int sub;
+};
+
+// Context shared by every launch of the library (per device).
+struct DeviceCtx {
+    int device = -1;
+    int num_sms = 0;
+    unsigned int* err_word = nullptr;   // device address of the sticky error word
+};
+const DeviceCtx* device_ctx();          // nullptr if no CUDA device is usable
+
+// ------------------------------------------------------ CUDA-core kernels
+// rows of W (N rows, length K, pitch ldw) dotted with nb tokens of X (pitch ldx);
+// W1 non-null only for EPI_SWIGLU (up weights, same shape as W).
+struct RowdotArgs {
+    const void* X;
+    int64_t ldx;
+    int nb;
+    const void* W;
+    const void* W1;
+    int64_t ldw;
+    int64_t N, K;
+    KSplit ks;
+    int64_t tok0;      // token offset added when storing
+    Epilogue epi;
+};
+cudaError_t launch_rowdot(const RowdotArgs& a, bool bf16, cudaStream_t st);
+
+// Sum of split partials ws[tp*sub, rows, cols] (fp32): per shard over its sub
+// chunks, then over shards in ascending order.  Optional outputs: the shard
+// partials [tp, rows, cols] fp32, and y = residual + sum written as dtype
+// (layout ALLREDUCE [rows, cols] or REDUCE_SCATTER [tp, rows, cols/tp]).
+// Optional norm_out = RMSNorm(bf16(y)) (bf16), which needs the whole row.
+struct ReduceArgs {
+    const float* ws;
+    int64_t rows, cols;
+    int tp, sub;
+    float* shard_out;
+    void* y;
+    int y_bf16;
+    int mode;              // tpl_reduce_mode
+    const void* residual;  // bf16 [rows, cols] or null
+    void* norm_out;        // bf16 [rows, cols] or null
+    float eps;
+    const float* ws_up;    // non-null: ws/ws_up are gate/up planes -> y = silu(sum ws) * sum ws_up
+    float* row_ss;         // norm_out only: [rows] sums of squares, zero on entry (reset on exit)
+    unsigned int* row_cnt; // norm_out only: [rows] block tickets, zero on entry (reset on exit)
+};
+cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
+
+// RMSNorm of bf16 rows (unit gain); zeroes row_ss/row_cnt itself.
+cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, float* row_ss,
+                           unsigned int* row_cnt, cudaStream_t st);
+
+// ---------------------------------------------------- tensor-core GEMM
+// D[M, N] = A[M, K] B[N, K]^T, A and B bf16 K-major.  `swap` means A holds the
+// weights (M = features) and B the tokens (N = tokens); otherwise A holds the
+// tokens.  A2 / B2: second weight operand for SwiGLU (up weights).
+struct TcGemmArgs {
+    const void* A;  int64_t lda;  int64_t M;
+    const void* B;  int64_t ldb;  int64_t N;
+    const void* A2; const void* B2;
+    int64_t K;
+    KSplit ks;
+    bool swap;
+    Epilogue epi;
+};
+bool tc_gemm_supported();
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st);
+
+}  // namespace tpl

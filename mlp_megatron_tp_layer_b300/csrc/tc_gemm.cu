@@ -1,0 +1,542 @@
+// Tensor-core GEMM for sm_103a: TMA loads into 128B-swizzled shared memory,
+// tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) issued by one thread into
+// a double-buffered TMEM accumulator, tcgen05.ld epilogue.  Persistent: one
+// CTA per SM walks a static tile list, so the load pipeline keeps streaming
+// across tile boundaries and the epilogue of tile i overlaps the MMAs of i+1.
+//
+//   D[M, N] = A[M, K] . B[N, K]^T     (both operands K-major, bf16)
+//
+// Normal orientation: A = activations (M = tokens), B = [out, in] weights.
+// Swapped orientation (decode, few tokens): A = weights (M = features, 128 per
+// tile), B = tokens (N = 16..128), so weights stream as the M=128 operand.
+// DUAL (SwiGLU): normal -> the B tile is [128 gate rows; 128 up rows] and one
+// N=256 MMA produces both; swapped -> two A tiles (gate, up) and two MMAs into
+// adjacent TMEM column ranges.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA sets
+// the sticky device error word, drains what it started, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace tpl {
+namespace {
+
+constexpr int BM = 128;             // rows of A per tile (TMEM lanes)
+constexpr int BK = 64;              // K elements per stage (128 bytes of bf16: one swizzle row)
+constexpr int kThreads = 192;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s: a healthy wait lasts microseconds
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  Returns false when the
+// time limit passes or another role has already aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive on `bar` once every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+#define TPL_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane base+i.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : TPL_R8(0), TPL_R8(8), TPL_R8(16), TPL_R8(24)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : TPL_R8(0), TPL_R8(8)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+#undef TPL_R8
+
+// Shared-memory matrix descriptor for a K-major operand tile stored as rows
+// of 128 bytes with the 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B): 8-row groups are 1024 bytes apart (SBO); the
+// leading offset is unused for this layout.  Advancing the start address by
+// 32 bytes selects the next 16-element K slice inside the swizzled row.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // bits  0-13 start address >> 4
+    d |= (uint64_t)(16u >> 4) << 16;                    // bits 16-29 leading byte offset >> 4
+    d |= (uint64_t)(1024u >> 4) << 32;                  // bits 32-45 stride byte offset >> 4
+    d |= (uint64_t)1 << 46;                             // bits 46-47 descriptor version 1
+    d |= (uint64_t)2 << 61;                             // bits 61-63 swizzle: 128B
+    return d;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4)                      // D format: f32
+         | (1u << 7)                      // A format: bf16
+         | (1u << 10)                     // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)     // N >> 3
+         | ((uint32_t)(M >> 4) << 24);    // M >> 4
+}
+
+struct TcParams {
+    int64_t M;            // valid rows of A (tokens, or features when swapped)
+    int64_t NB;           // valid rows of each B operand (features, hidden units, or tokens)
+    int m_tiles, n_tiles, splits;
+    int64_t total_tiles;
+    KSplit ks;
+    Epilogue epi;
+    unsigned int* err;
+};
+
+template <int BN, bool SWAP, bool DUAL>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;                          // 16 KB
+    static constexpr int A2_BYTES = (SWAP && DUAL) ? A_BYTES : 0;
+    static constexpr int B_BYTES = BN * BK * 2;                          // includes gate+up when normal DUAL
+    static constexpr int STAGE_BYTES = A_BYTES + A2_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
+    static constexpr int B_ROWS = (!SWAP && DUAL) ? BN / 2 : BN;         // rows per B TMA box
+    static constexpr int ACC_COLS = (SWAP && DUAL) ? 2 * BN : BN;        // TMEM columns per accumulator
+    static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32) ? 32 : (2 * ACC_COLS <= 64) ? 64
+                                   : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
+    static constexpr int OUT_COLS = (!SWAP && DUAL) ? BN / 2 : BN;       // output columns per tile
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static_assert(2 * ACC_COLS <= 512, "TMEM holds 512 fp32 columns");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N in 16..256 step 16");
+};
+
+struct TileCoord { int sp, mt, nt; };
+__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int64_t t) {
+    const int64_t per_split = (int64_t)p.m_tiles * p.n_tiles;
+    TileCoord c;
+    c.sp = (int)(t / per_split);
+    const int64_t r = t - (int64_t)c.sp * per_split;
+    c.mt = (int)(r % p.m_tiles);      // m fastest: concurrent CTAs share the B (weight) tile
+    c.nt = (int)(r / p.m_tiles);
+    return c;
+}
+__device__ __forceinline__ void split_range(const TcParams& p, int sp, int64_t& k0, int& nkb) {
+    const int sh = sp / p.ks.sub, j = sp - sh * p.ks.sub;
+    k0 = sh * p.ks.k_shard + (int64_t)j * p.ks.k_chunk;
+    const int64_t k1 = min(k0 + p.ks.k_chunk, (int64_t)(sh + 1) * p.ks.k_shard);
+    nkb = (int)((k1 - k0 + BK - 1) / BK);
+}
+
+template <int BN, bool SWAP, bool DUAL>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+               const TcParams p) {
+    using C = Cfg<BN, SWAP, DUAL>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* acc_full = bars + 2 * C::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // zero the row accumulators of the reduction that will consume this output
+    if (p.epi.zero_words && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.epi.zero_count; i += blockDim.x) p.epi.zero_words[i] = 0u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&acc_full[a]), 1);
+            mbar_init(smem_addr(&acc_empty[a]), 4);
+        }
+        mbar_init(smem_addr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (DUAL) { if (SWAP) prefetch_tmap(&tmA2); else prefetch_tmap(&tmB2); }
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.err) atomicOr(p.err, TPL_DEVERR_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_tail = 0;   // stages loaded but not yet known to be consumed (abort drain)
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                const TileCoord c = tile_coord(p, t);
+                int64_t k0;
+                int nkb;
+                split_range(p, c.sp, k0, nkb);
+                const int am = c.mt * BM;
+                const int bn = c.nt * C::B_ROWS;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(smem_addr(&empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    mbar_expect_tx(fb, C::STAGE_BYTES);
+                    uint8_t* st = smem + stage * C::STAGE_BYTES;
+                    const int kx = (int)(k0 + kb * BK);
+                    if (SWAP) {
+                        tma_load_hint(smem_addr(st), &tmA, fb, kx, am, pol_w);
+                        if (DUAL) tma_load_hint(smem_addr(st + C::A_BYTES), &tmA2, fb, kx, am, pol_w);
+                        tma_load_hint(smem_addr(st + C::A_BYTES + C::A2_BYTES), &tmB, fb, kx, bn, pol_x);
+                    } else {
+                        tma_load(smem_addr(st), &tmA, fb, kx, am);
+                        tma_load(smem_addr(st + C::A_BYTES), &tmB, fb, kx, bn);
+                        if (DUAL) tma_load(smem_addr(st + C::A_BYTES + C::B_BYTES / 2), &tmB2, fb, kx, bn);
+                    }
+                    issued_tail = min(issued_tail + 1, C::STAGES);
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                fail();
+                // Let the copies already issued land before the CTA exits: wait
+                // (bounded) on the full barrier of each in-flight stage.
+                for (int i = 0; i < issued_tail; ++i) {
+                    if (--stage < 0) { stage = C::STAGES - 1; phase ^= 1; }
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_addr(&full[stage]), phase) && globaltimer() - t0 < kTimeoutNs) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, (SWAP || !DUAL) ? BN : BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+                const TileCoord c = tile_coord(p, t);
+                int64_t k0;
+                int nkb;
+                split_range(p, c.sp, k0, nkb);
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * C::ACC_COLS;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(smem_addr(&full[stage]), phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + C::A_BYTES + C::A2_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t accum = (kb | kk) ? 1u : 0u;
+                        mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc, accum);
+                        if (SWAP && DUAL)
+                            mma_bf16(d + BN, sw128_desc(sa + C::A_BYTES + kk * 32), sw128_desc(sb + kk * 32),
+                                     idesc, accum);
+                    }
+                    mma_commit(smem_addr(&empty[stage]));
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_addr(&acc_full[acc]));
+            }
+            if (!ok) fail();
+            // Wait (bounded) until every MMA issued above has completed, so TMEM
+            // can be released safely.
+            mma_commit(smem_addr(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_addr(drain), 0) && globaltimer() - t0 < kTimeoutNs) {}
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+            const TileCoord c = tile_coord(p, t);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            // every lane polls; the vote keeps the warp converged for the
+            // .sync.aligned TMEM loads even when a wait gives up
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&acc_full[acc]), acc_phase, abort_flag));
+            if (!ok) { if (lane == 0) fail(); break; }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
+            const int64_t a_row = (int64_t)c.mt * BM + row;         // token (normal) or feature (swapped)
+            constexpr int CH = C::OUT_COLS >= 32 ? 32 : 16;
+            float v[32], u[32];
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::OUT_COLS; c0 += CH) {
+                if (CH == 32) tmem_ld32(tbase + c0, v); else tmem_ld16(tbase + c0, v);
+                if (DUAL) {
+                    const int up_off = SWAP ? BN : BN / 2;
+                    if (CH == 32) tmem_ld32(tbase + up_off + c0, u); else tmem_ld16(tbase + up_off + c0, u);
+                }
+                if (a_row < p.M) {
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const int64_t b_row = (int64_t)c.nt * C::OUT_COLS + c0 + j;
+                        if (b_row < p.NB) {
+                            const int64_t tok = SWAP ? b_row : a_row;
+                            const int64_t feat = SWAP ? a_row : b_row;
+                            if (DUAL) store_pair(p.epi, c.sp, tok, feat, v[j], u[j]);
+                            else store_value(p.epi, c.sp, tok, feat, v[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&acc_empty[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] with row pitch ld (elements); box = 64 x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Tensor maps are pure functions of (pointer, shape, box); cache them so a
+// decode step does not re-encode the same weights on every call.
+struct MapKey {
+    const void* base; int64_t rows, cols, ld; int box;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && box == o.box;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.base);
+        h ^= std::hash<int64_t>()(k.rows * 1000003 + k.cols * 31 + k.ld * 7 + k.box) + 0x9e3779b97f4a7c15ull + (h << 6);
+        return h;
+    }
+};
+bool cached_map(CUtensorMap* out, const void* base, int64_t rows, int64_t cols, int64_t ld, int box) {
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    MapKey k{base, rows, cols, ld, box};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(k);
+    if (it != cache.end()) { *out = it->second; return true; }
+    if (!make_map(out, base, rows, cols, ld, box)) return false;
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(k, *out);
+    return true;
+}
+
+template <int BN, bool SWAP, bool DUAL>
+cudaError_t launch_cfg(const TcGemmArgs& a, cudaStream_t st) {
+    using C = Cfg<BN, SWAP, DUAL>;
+    const DeviceCtx* ctx = device_ctx();
+    if (!ctx) return cudaErrorNoDevice;
+    static bool attr_set[64] = {};
+    const int dev = ctx->device;
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, SWAP, DUAL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    CUtensorMap mA, mA2, mB, mB2;
+    const int a_box = BM;
+    const int b_box = C::B_ROWS;
+    if (!cached_map(&mA, a.A, a.M, a.K, a.lda, a_box)) return cudaErrorInvalidValue;
+    if (!cached_map(&mB, a.B, a.N, a.K, a.ldb, b_box)) return cudaErrorInvalidValue;
+    mA2 = mA;
+    mB2 = mB;
+    if (DUAL && SWAP && !cached_map(&mA2, a.A2, a.M, a.K, a.lda, a_box)) return cudaErrorInvalidValue;
+    if (DUAL && !SWAP && !cached_map(&mB2, a.B2, a.N, a.K, a.ldb, b_box)) return cudaErrorInvalidValue;
+
+    TcParams p;
+    p.M = a.M;
+    p.NB = a.N;
+    p.m_tiles = (int)((a.M + BM - 1) / BM);
+    p.n_tiles = (int)((a.N + C::OUT_COLS - 1) / C::OUT_COLS);
+    p.splits = a.ks.tp * a.ks.sub;
+    p.total_tiles = (int64_t)p.m_tiles * p.n_tiles * p.splits;
+    p.ks = a.ks;
+    p.epi = a.epi;
+    p.err = ctx->err_word;
+    const int64_t grid = std::min<int64_t>(p.total_tiles, ctx->num_sms);
+    tc_gemm_kernel<BN, SWAP, DUAL><<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(mA, mA2, mB, mB2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_gemm_supported() {
+    const DeviceCtx* ctx = device_ctx();
+    if (!ctx) return false;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+    return major == 10 && minor == 3 && get_encoder() != nullptr;
+}
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st) {
+    const bool dual = a.epi.mode == EPI_SWIGLU || a.epi.mode == EPI_PARTIAL2;
+    if (!a.swap) {
+        return dual ? launch_cfg<256, false, true>(a, st) : launch_cfg<256, false, false>(a, st);
+    }
+    // swapped: tile N covers the tokens
+    if (a.N <= 16) return dual ? launch_cfg<16, true, true>(a, st) : launch_cfg<16, true, false>(a, st);
+    if (a.N <= 32) return dual ? launch_cfg<32, true, true>(a, st) : launch_cfg<32, true, false>(a, st);
+    if (a.N <= 64) return dual ? launch_cfg<64, true, true>(a, st) : launch_cfg<64, true, false>(a, st);
+    return dual ? launch_cfg<128, true, true>(a, st) : launch_cfg<128, true, false>(a, st);
+}
+
+}  // namespace tpl

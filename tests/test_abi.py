@@ -1,0 +1,85 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports
+every function include/tpl.h declares, and rejects bad arguments with the
+documented status codes before touching any device."""
+import ctypes
+
+import pytest
+
+tpl = pytest.importorskip("mlp_megatron_tp_layer_b300")
+lib = tpl.lib
+NULL = None
+
+
+def test_every_declared_symbol_is_exported():
+    names = tpl.header_functions()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_status_strings_and_version():
+    for code in range(10):
+        assert lib.tpl_status_string(code)
+    assert lib.tpl_status_string(12345) == b"unknown status"
+    assert lib.tpl_version() >> 16 == 1
+
+
+def _ws(fn, *args):
+    n = ctypes.c_size_t(0)
+    st = fn(*args, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_queries_and_shape_errors():
+    st, n = _ws(lib.tpl_tp_mlp_forward_workspace, 64, 1536, 8960, 2, tpl.BF16)
+    assert st == 0 and n >= 64 * 8960 * 2
+    assert _ws(lib.tpl_tp_mlp_forward_workspace, 64, 1536, 8960, 3, tpl.BF16)[0] == 2      # F % tp
+    assert _ws(lib.tpl_tp_mlp_forward_workspace, 0, 1536, 8960, 2, tpl.BF16)[0] == 2       # B <= 0
+    assert _ws(lib.tpl_tp_mlp_forward_workspace, 4, 1532, 8960, 2, tpl.BF16)[0] == 3       # D row not 16 B
+    assert _ws(lib.tpl_tp_mlp_forward_workspace, 4, 1536, 8960, 2, 7)[0] == 4              # dtype
+    assert lib.tpl_tp_mlp_forward_workspace(4, 1536, 8960, 2, 1, None) == 1                # null out
+    st, n = _ws(lib.tpl_tp_attn_proj_workspace, 8, 1536, 12, 2, 128, 2, tpl.BF16)
+    assert st == 0 and n > 0
+    assert _ws(lib.tpl_tp_attn_proj_workspace, 8, 1536, 12, 2, 128, 5, tpl.BF16)[0] == 2   # n_q % tp
+    assert _ws(lib.tpl_tp_attn_proj_workspace, 8, 1536, 12, 4, 128, 6, tpl.BF16)[0] == 2   # tp > n_kv, tp % n_kv
+    assert _ws(lib.tpl_tp_attn_proj_workspace, 8, 1536, 12, 2, 128, 4, tpl.BF16)[0] == 0   # replicated KV ok
+    assert _ws(lib.tpl_sharded_matmul_workspace, 3, 0, 512, 8192, 28672, 8, tpl.BF16)[0] == 0
+    assert _ws(lib.tpl_sharded_matmul_workspace, 1, 0, 500, 8192, 28672, 8, tpl.BF16)[0] == 2   # I % X case 1
+    assert _ws(lib.tpl_sharded_matmul_workspace, 3, 0, 500, 8192, 28672, 8, tpl.BF16)[0] == 0   # I free in case 3
+    assert _ws(lib.tpl_sharded_matmul_workspace, 5, 0, 512, 8192, 28672, 8, tpl.BF16)[0] == 6   # no case 5
+    assert _ws(lib.tpl_tp_decoder_workspace, 8, 8192, 28672, 64, 8, 128, 8)[0] == 0
+
+
+def test_calls_reject_null_and_misaligned_pointers_without_launching():
+    s = ctypes.c_void_p(0)
+    good = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    # null pointers
+    assert lib.tpl_shard_reduce(NULL, good, 4, 8, 2, 0, 1, s) == 1
+    assert lib.tpl_tp_mlp_forward(good, good, NULL, good, good, NULL, 8, 256, 1024, 2, 1, 1, good, 1 << 30, s) == 1
+    assert lib.tpl_tp_attn_proj(NULL, good, good, NULL, good, NULL, 8, 256, 4, 2, 64, 2, 1, 1, good, 1 << 30, s) == 1
+    assert lib.tpl_sharded_matmul(1, 0, 0, good, NULL, good, NULL, 8, 64, 64, 2, 1, 1, good, 1 << 30, s) == 1
+    # misaligned pointers
+    assert lib.tpl_shard_reduce(bad, good, 4, 8, 2, 0, 1, s) == 3
+    assert lib.tpl_tp_mlp_forward(good, good, good, bad, ctypes.c_void_p(2 << 20), NULL, 8, 256, 1024, 2, 1, 1,
+                                  ctypes.c_void_p(3 << 20), 1 << 30, s) == 3
+    # bad dtype combination: fp32 inputs with a bf16 output
+    assert lib.tpl_tp_mlp_forward(good, good, good, good, good, NULL, 8, 256, 1024, 2, 0, 1, good, 1 << 30, s) == 4
+    # shape errors come before anything else that needs a device
+    assert lib.tpl_shard_reduce(good, ctypes.c_void_p(2 << 20), 4, 9, 2, 1, 1, s) == 2   # RS needs cols % tp
+    assert lib.tpl_shard_reduce(good, ctypes.c_void_p(2 << 20), 4, 8, 2, 9, 1, s) == 6   # bad mode
+
+
+def test_overlapping_output_is_rejected():
+    s = ctypes.c_void_p(0)
+    base = 1 << 24
+    # Y overlaps X
+    st = lib.tpl_tp_mlp_forward(ctypes.c_void_p(base), ctypes.c_void_p(2 * base), ctypes.c_void_p(3 * base),
+                                ctypes.c_void_p(4 * base), ctypes.c_void_p(base + 256), None, 8, 256, 1024, 2, 1,
+                                1, ctypes.c_void_p(5 * base), 1 << 30, s)
+    assert st == 9
+    # workspace too small
+    st = lib.tpl_tp_mlp_forward(ctypes.c_void_p(base), ctypes.c_void_p(2 * base), ctypes.c_void_p(3 * base),
+                                ctypes.c_void_p(4 * base), ctypes.c_void_p(6 * base), None, 8, 256, 1024, 2, 1,
+                                1, ctypes.c_void_p(5 * base), 16, s)
+    assert st == 5
