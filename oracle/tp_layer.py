@@ -370,10 +370,13 @@ def rmsnorm(x, eps: float = RMS_EPS) -> np.ndarray:
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
 
 
-def decoder_layer(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, sharded: bool = True):
+def decoder_layer(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, sharded: bool = True,
+                  trace: list | None = None):
     """h = x + Attn(RMSNorm(x));  y = h + MLP(RMSNorm(h)); bf16 between steps.
 
     ``W`` holds Wqkv, Wo, Wg, Wu, Wd.  Returns y (bf16 values, float64 array).
+    If ``trace`` is a list, the two rounded residual-stream values h and y are
+    appended to it (read-only instrumentation; the arithmetic is unchanged).
     """
     xn = bf16_round(rmsnorm(x))
     if sharded:
@@ -388,7 +391,10 @@ def decoder_layer(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, shard
         m_sum = shard_reduce(P, False)
     else:
         m_sum = linear(bf16_round(silu(linear(hn, W["Wg"])) * linear(hn, W["Wu"])), W["Wd"])
-    return bf16_round(h + m_sum)
+    y = bf16_round(h + m_sum)
+    if trace is not None:
+        trace.extend([h, y])
+    return y
 
 
 def linear_attn_sum(xn, W, n_q, n_kv, head_dim):
@@ -402,9 +408,11 @@ def linear_attn_sum(xn, W, n_q, n_kv, head_dim):
     return linear(O, W["Wo"])
 
 
-def decoder_stack(x, layers: list, n_q: int, n_kv: int, head_dim: int, tp: int, sharded: bool = True):
-    """Layers applied in order; returns the final residual stream (bf16 values)."""
+def decoder_stack(x, layers: list, n_q: int, n_kv: int, head_dim: int, tp: int, sharded: bool = True,
+                  trace: list | None = None):
+    """Layers applied in order; returns the final residual stream (bf16 values).
+    ``trace`` as in decoder_layer: every rounded residual-stream value, in order."""
     y = bf16_round(x)
     for W in layers:
-        y = decoder_layer(y, W, n_q, n_kv, head_dim, tp, sharded)
+        y = decoder_layer(y, W, n_q, n_kv, head_dim, tp, sharded, trace)
     return y

@@ -8,7 +8,7 @@ import torch
 
 import synthetic_inputs as si
 from oracle import tp_layer as O
-from tests.helpers import F32_REL, assert_close, assert_equal, to_np
+from tests.helpers import F32_REL, assert_close, assert_equal, assert_within, stack_allowance, to_np
 
 pytestmark = pytest.mark.gpu
 tpl = pytest.importorskip("mlp_megatron_tp_layer_b300")
@@ -210,9 +210,14 @@ def test_decoder_stack_small(B):
     D, F, n_q, n_kv, hd, tp, L = 256, 512, 4, 2, 64, 2, 3
     x = si.activations(B, D, seed=5, device="cuda")
     layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=5, layer=l, sigma=0.05, device="cuda") for l in range(L)]
-    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp)
+    trace = []
+    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                          trace=trace)
     y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp)
-    assert_close(y, ref, bf16_out=True, what="stack output")
+    # one layer: the stated bar plus the bf16 roundings of h and y
+    y1 = tpl.tp_decoder_stack(x, layers[:1], n_q, n_kv, hd, tp)
+    assert_within(y1, trace[1], stack_allowance(trace[:2], trace[1]), what="first layer")
+    assert_within(y, ref, stack_allowance(trace, ref), what="stack output")
     # the stack equals the layer-by-layer composition bit for bit
     z = x
     for W in layers:
