@@ -278,8 +278,8 @@ def main():
     eager_step()
     torch.cuda.synchronize()
     recs = profile_pass(tpl, eager_step, stream)
-    # launch_rmsnorm scopes also hold two small zeroing kernels
-    launches_per_step = len(recs) + 2 * sum(1 for t, _ in recs if t == "rmsnorm")
+    # launch_rmsnorm scopes also hold one small zeroing kernel
+    launches_per_step = len(recs) + sum(1 for t, _ in recs if t == "rmsnorm")
 
     # CUDA graphs: one per batch size, replaying the library's launches
     graphs = {}

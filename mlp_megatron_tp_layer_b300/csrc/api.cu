@@ -209,13 +209,14 @@ Epilogue epi_store(void* out, int bf16, int64_t ldo) {
     e.mode = EPI_STORE; e.out = out; e.out_bf16 = bf16; e.ldo = ldo;
     return e;
 }
-// rowacc (optional): [2 * rows] words the consuming reduction uses; zeroed by this launch.
+// rowacc (optional): the consuming row-normalising reduction's tickets ([rows]
+// words at its start), zeroed by this launch.
 Epilogue epi_partial(float* out32, int64_t ldo, int64_t split_stride, unsigned int* rowacc = nullptr,
                      int64_t rows = 0) {
     Epilogue e{};
     e.mode = EPI_PARTIAL; e.out32 = out32; e.ldo = ldo; e.split_stride = split_stride;
     e.zero_words = rowacc;
-    e.zero_count = rowacc ? (int)(2 * rows) : 0;
+    e.zero_count = rowacc ? (int)rows : 0;
     return e;
 }
 
@@ -272,8 +273,8 @@ cudaError_t reduce_into(const float* ws, int64_t rows, int64_t cols, const KSpli
     r.norm_out = norm_out;
     r.eps = kRmsEps;
     r.ws_up = nullptr;
-    r.row_ss = rowacc ? reinterpret_cast<float*>(rowacc) : nullptr;
-    r.row_cnt = rowacc ? rowacc + rows : nullptr;
+    r.row_cnt = rowacc;
+    r.row_slots = rowacc ? reinterpret_cast<float*>(rowacc + rows) : nullptr;
     ProfScope prof(norm_out ? "reduce_norm" : "reduce", st);
     return launch_reduce(r, st);
 }
@@ -385,8 +386,8 @@ LayerPlan plan_layer(int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int hd,
     p.xn_off = 0;
     p.h_off = act;
     p.hn_off = 2 * act;
-    p.acc_off = 3 * act;                            // [2 B] row accumulators of the norm reductions
-    p.attn_off = p.acc_off + up((size_t)B * 8);
+    p.acc_off = 3 * act;                            // row accumulators of the norm reductions
+    p.attn_off = p.acc_off + up(rowacc_bytes(B, D));
     const size_t attn = plan_attn(B, D, n_q, n_kv, hd, tp, TPL_BF16).total;
     p.mlp_off = p.attn_off + up(attn);
     p.total = p.mlp_off + up(plan_mlp(B, D, F, tp, TPL_BF16, false).total);
@@ -404,7 +405,7 @@ cudaError_t run_layer(const void* x, void* y, const void* Wqkv, const void* Wo, 
     cudaError_t err;
     if (!x_normed_ready) {
         ProfScope prof("rmsnorm", st);
-        err = launch_rmsnorm(x, xn, B, D, kRmsEps, reinterpret_cast<float*>(rowacc), rowacc + B, st);
+        err = launch_rmsnorm(x, xn, B, D, kRmsEps, rowacc, st);
         if (err != cudaSuccess) return err;
     }
     // attention sublayer: h = x + sum_s P_s, hn = RMSNorm(h)

@@ -98,14 +98,21 @@ struct ReduceArgs {
     void* norm_out;        // bf16 [rows, cols] or null
     float eps;
     const float* ws_up;    // non-null: ws/ws_up are gate/up planes -> y = silu(sum ws) * sum ws_up
-    float* row_ss;         // norm_out only: [rows] sums of squares, zero on entry (reset on exit)
     unsigned int* row_cnt; // norm_out only: [rows] block tickets, zero on entry (reset on exit)
+    float* row_slots;      // norm_out only: [rows, norm_blocks(cols)] per-block sums of squares
 };
+
+// The row-normalising reduction covers kNormCols columns per block; a row's
+// sum of squares is the sum of its blocks' slots in block order (deterministic).
+// Row accumulator area ("rowacc") used by it: [rows] tickets, then the slots.
+constexpr int kNormCols = 512;
+inline int64_t norm_blocks(int64_t cols) { return (cols + kNormCols - 1) / kNormCols; }
+inline size_t rowacc_bytes(int64_t rows, int64_t cols) { return (size_t)rows * 4 * (1 + norm_blocks(cols)); }
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
 
-// RMSNorm of bf16 rows (unit gain); zeroes row_ss/row_cnt itself.
-cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, float* row_ss,
-                           unsigned int* row_cnt, cudaStream_t st);
+// RMSNorm of bf16 rows (unit gain); zeroes the tickets of rowacc itself.
+cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, unsigned int* rowacc,
+                           cudaStream_t st);
 
 // ---------------------------------------------------- tensor-core GEMM
 // D[M, N] = A[M, K] B[N, K]^T, A and B bf16 K-major.  `swap` means A holds the

@@ -219,7 +219,7 @@ __global__ void reduce_kernel(const ReduceArgs a) {
     }
 }
 
-constexpr int kNormThreads = 128;               // 4 columns per thread: 512 columns per block
+constexpr int kNormThreads = kNormCols / 4;     // 4 columns per thread
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
@@ -234,12 +234,13 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // Grid (column blocks, rows).  Each block: y = bf16(residual + sum of
-// partials) for its 512 columns (or y = x when tp == 0), and its share of the
-// row's sum of squares of the ROUNDED values.  The last block of a row to
-// finish (atomic ticket; nothing waits) scales the whole row:
-// norm_out = bf16(y / sqrt(mean(y^2) + eps)).  row_ss / row_cnt start at zero
-// (the kernel that produced the partials zeroes them) and the last block
-// resets them.
+// partials) for its kNormCols columns (or y = x when tp == 0), and its share of
+// the row's sum of squares of the ROUNDED values, written to its own slot.  The
+// last block of a row to finish (atomic ticket; nothing waits) adds the slots
+// in block order -- the same sum whatever order the blocks ran in -- and
+// scales the whole row: norm_out = bf16(y / sqrt(mean(y^2) + eps)).  row_cnt
+// starts at zero (the kernel that produced the partials zeroes it) and the
+// last block resets it.
 __global__ void __launch_bounds__(kNormThreads) reduce_norm_kernel(const ReduceArgs a) {
     const int64_t row = blockIdx.y;
     const int64_t n = a.rows * a.cols;
@@ -276,16 +277,18 @@ __global__ void __launch_bounds__(kNormThreads) reduce_norm_kernel(const ReduceA
         }
     }
     const float bsum = block_sum(ss, red);
+    float* slots = a.row_slots + row * gridDim.x;
     if (threadIdx.x == 0) {
-        atomicAdd(a.row_ss + row, bsum);
+        slots[blockIdx.x] = bsum;
         __threadfence();
         ticket = atomicAdd(a.row_cnt + row, 1u);
     }
     __syncthreads();
     if (ticket != gridDim.x - 1) return;
-    // last block of this row: every other block's y and partial sum are visible
+    // last block of this row: every other block's y and slot are visible
     __threadfence();
-    const float total = atomicAdd(a.row_ss + row, 0.0f);
+    float total = 0.f;
+    for (unsigned b = 0; b < gridDim.x; ++b) total += __ldcg(slots + b);
     const float scale = 1.0f / sqrtf(total / (float)a.cols + a.eps);
     const __nv_bfloat16* src = y ? y : res;     // y == null only for the plain RMSNorm (tp == 0)
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.norm_out);
@@ -301,10 +304,7 @@ __global__ void __launch_bounds__(kNormThreads) reduce_norm_kernel(const ReduceA
               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[3] * scale)) << 16);
         *reinterpret_cast<uint2*>(out + i) = w;
     }
-    if (threadIdx.x == 0) {
-        a.row_ss[row] = 0.f;
-        a.row_cnt[row] = 0u;
-    }
+    if (threadIdx.x == 0) a.row_cnt[row] = 0u;
 }
 
 // Zero the row accumulators before a plain RMSNorm (no producing GEMM precedes it).
@@ -323,7 +323,7 @@ cudaError_t launch_rowdot(const RowdotArgs& a, bool bf16, cudaStream_t st) {
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
     if (a.norm_out) {
-        dim3 grid((unsigned)((a.cols + 4 * kNormThreads - 1) / (4 * kNormThreads)), (unsigned)a.rows);
+        dim3 grid((unsigned)norm_blocks(a.cols), (unsigned)a.rows);
         reduce_norm_kernel<<<grid, kNormThreads, 0, st>>>(a);
         return cudaGetLastError();
     }
@@ -335,10 +335,9 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, float* row_ss,
-                           unsigned int* row_cnt, cudaStream_t st) {
-    zero_words_kernel<<<1, 256, 0, st>>>(reinterpret_cast<unsigned int*>(row_ss), (int)rows);
-    zero_words_kernel<<<1, 256, 0, st>>>(row_cnt, (int)rows);
+cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, unsigned int* rowacc,
+                           cudaStream_t st) {
+    zero_words_kernel<<<1, 256, 0, st>>>(rowacc, (int)rows);
     ReduceArgs a{};
     a.ws = nullptr;
     a.rows = rows;
@@ -349,8 +348,8 @@ cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, f
     a.y = nullptr;
     a.norm_out = y;
     a.eps = eps;
-    a.row_ss = row_ss;
-    a.row_cnt = row_cnt;
+    a.row_cnt = rowacc;
+    a.row_slots = reinterpret_cast<float*>(rowacc + rows);
     return launch_reduce(a, st);
 }
 
