@@ -68,7 +68,9 @@ typedef enum tpl_status {
     TPL_ERR_UNSUPPORTED = 6,  /* argument combination not supported (see the call)  */
     TPL_ERR_CUDA = 7,         /* the CUDA runtime reported an error                 */
     TPL_ERR_TIMEOUT = 8,      /* a device-side bounded wait gave up                 */
-    TPL_ERR_ALIAS = 9         /* an output buffer overlaps an input buffer          */
+    TPL_ERR_ALIAS = 9,        /* an output buffer overlaps an input buffer          */
+    TPL_ERR_STATIC_LIMIT = 10 /* the problem needs more scratch than the library's
+                                 static device area (TPL_STATIC_WS_BYTES) holds    */
 } tpl_status;
 
 typedef enum tpl_dtype { TPL_F32 = 0, TPL_BF16 = 1 } tpl_dtype;
@@ -131,6 +133,41 @@ tpl_status tpl_tp_mlp_forward_workspace(int64_t B, int64_t D, int64_t F, int tp,
 tpl_status tpl_tp_mlp_forward(const void* X, const void* Wg, const void* Wu, const void* Wd,
                               void* Y, float* partials, int64_t B, int64_t D, int64_t F, int tp,
                               int dtype, int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * tp_mlp_forward_static_ws -- tp_mlp_forward for callers that cannot allocate
+ * device memory.  The reference pages have no counterpart: this is a service
+ * of this library, not a step of the method.
+ *
+ * Some callers have no device buffer to give as `ws`: a serving loop that has
+ * handed all of HBM to its own pool (KV cache, weights), code that must not
+ * call cudaMalloc because it synchronises the device or would break a stream
+ * capture in progress, or a host that links this library without any
+ * allocator of its own.  This entry point takes the same arguments as
+ * tp_mlp_forward minus ws / ws_bytes and runs the same kernels, with scratch
+ * taken from a static __device__ array inside the library of
+ * TPL_STATIC_WS_BYTES (32 MiB).  Every GPU on which the library is loaded
+ * holds that array until the process exits.
+ *   - The caller still owns and passes X, the weights, Y and the optional
+ *     partials.  No device memory is allocated or freed by this call.
+ *   - The problem's workspace (tp_mlp_forward_workspace) must fit in
+ *     TPL_STATIC_WS_BYTES, else TPL_ERR_STATIC_LIMIT and nothing is launched.
+ *     Decode-sized calls fit, e.g. D 1536, F 8960 (tp 2) up to B = 128 and
+ *     D 8192, F 28672 (tp 8) up to B = 32; a 4096-token prefill of the latter
+ *     (352 MiB of workspace) does not.
+ *   - All calls on a device share the one array, which keeps what the last
+ *     call left in it (nothing in it needs to start at zero).  Calls whose
+ *     kernels overlap on the GPU -- on different streams or from different
+ *     host threads without ordering -- race on it; order them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture that includes this call.
+ * ------------------------------------------------------------------------ */
+#define TPL_STATIC_WS_BYTES (32u << 20)
+tpl_status tpl_tp_mlp_forward_static_ws(const void* X, const void* Wg, const void* Wu,
+                                        const void* Wd, void* Y, float* partials, int64_t B,
+                                        int64_t D, int64_t F, int tp, int dtype, int out_dtype,
+                                        void* stream);
 
 /* --------------------------------------------------------------------------
  * tp_attn_proj -- attention projections split by head ([L4] S4.2, S4.4).

@@ -25,7 +25,8 @@ ALLREDUCE, REDUCE_SCATTER = 0, 1
 GATHER_B, GATHER_A = 0, 1
 STATUS = {0: "TPL_OK", 1: "TPL_ERR_NULL", 2: "TPL_ERR_SHAPE", 3: "TPL_ERR_ALIGN", 4: "TPL_ERR_DTYPE",
           5: "TPL_ERR_WORKSPACE", 6: "TPL_ERR_UNSUPPORTED", 7: "TPL_ERR_CUDA", 8: "TPL_ERR_TIMEOUT",
-          9: "TPL_ERR_ALIAS"}
+          9: "TPL_ERR_ALIAS", 10: "TPL_ERR_STATIC_LIMIT"}
+STATIC_WS_BYTES = 32 << 20
 
 _vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
@@ -36,6 +37,8 @@ _SIGS = {
     "tpl_tp_mlp_forward_workspace": (_i32, [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
     "tpl_tp_mlp_forward": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
                                   _vp, _sz, _vp]),
+    "tpl_tp_mlp_forward_static_ws": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
+                                            _vp]),
     "tpl_tp_attn_proj_workspace": (_i32, [_i64, _i64, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tpl_tp_attn_proj": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                                 _i32, _vp, _sz, _vp]),
@@ -189,6 +192,27 @@ def tp_mlp_forward(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=No
     ws = workspace(nbytes, X.device) if ws is None else ws
     _check(lib.tpl_tp_mlp_forward(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp, dt, odt,
                                   _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "tpl_tp_mlp_forward")
+    return (out, partials) if want else out
+
+
+def tp_mlp_forward_static_ws(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=None, stream=None):
+    """tp_mlp_forward with the library's static device scratch instead of a
+    workspace: for callers that cannot allocate device memory (see
+    tpl_tp_mlp_forward_static_ws in include/tpl.h for the limit and sharing)."""
+    _contig(X, Wg, Wu, Wd)
+    B, D = X.shape
+    F = Wg.shape[0]
+    dt = _dt(X)
+    odt = _out_code(dt, out, out_dtype)
+    if out is None:
+        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
+    want = partials is not None and partials is not False
+    if partials is True:
+        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
+    elif not want:
+        partials = None
+    _check(lib.tpl_tp_mlp_forward_static_ws(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp, dt,
+                                            odt, _stream(stream)), "tpl_tp_mlp_forward_static_ws")
     return (out, partials) if want else out
 
 

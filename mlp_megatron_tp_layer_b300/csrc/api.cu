@@ -435,6 +435,7 @@ extern "C" const char* tpl_status_string(int s) {
     case TPL_ERR_CUDA: return "CUDA runtime error";
     case TPL_ERR_TIMEOUT: return "device-side wait timed out";
     case TPL_ERR_ALIAS: return "output overlaps an input";
+    case TPL_ERR_STATIC_LIMIT: return "problem needs more scratch than the library's static device area holds";
     default: return "unknown status";
     }
 }

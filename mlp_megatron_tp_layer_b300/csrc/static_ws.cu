@@ -1,0 +1,53 @@
+// tp_mlp_forward with the library's own static device scratch instead of a
+// caller-provided workspace, for callers that cannot allocate device memory.
+//
+// The scratch is a file-scope __device__ array.  Its host-side name is only a
+// stand-in for the symbol, not a device address, so host code never passes it
+// to a kernel: the device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and cached.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_ws[TPL_STATIC_WS_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_ws on the current device (nullptr on error).
+// The first call on a device does the lookup; later calls return the cache.
+void* static_ws_address() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return nullptr;
+        g_static_ptr[dev] = p;
+    }
+    return g_static_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" tpl_status tpl_tp_mlp_forward_static_ws(const void* X, const void* Wg, const void* Wu, const void* Wd,
+                                                   void* Y, float* partials, int64_t B, int64_t D, int64_t F,
+                                                   int tp, int dtype, int out_dtype, void* stream) {
+    if (!X || !Wg || !Wu || !Wd || !Y) return TPL_ERR_NULL;
+    size_t need = 0;
+    const tpl_status s = tpl_tp_mlp_forward_workspace(B, D, F, tp, dtype, &need);
+    if (s != TPL_OK) return s;
+    if (need > (size_t)TPL_STATIC_WS_BYTES) return TPL_ERR_STATIC_LIMIT;
+    void* ws = static_ws_address();
+    if (!ws) return TPL_ERR_CUDA;
+    // Nothing in the MLP's scratch has to start at zero: every element of the
+    // hidden activations and of the split partials is written before it is
+    // read, so what an earlier call left in the array does not matter.
+    return tpl_tp_mlp_forward(X, Wg, Wu, Wd, Y, partials, B, D, F, tp, dtype, out_dtype, ws,
+                              (size_t)TPL_STATIC_WS_BYTES, stream);
+}
