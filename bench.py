@@ -58,6 +58,10 @@ def args_parse():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="run one workload only (small cases for profiling); prints that workload's line")
+    ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
+    ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
     return ap.parse_args()
 
 
@@ -247,17 +251,10 @@ def profile_pass(tpl, fn, stream):
     return rec
 
 
-def main():
-    args = args_parse()
-    rank, world = dist_init()
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
-    import mlp_megatron_tp_layer_b300 as tpl
-    dev = torch.device("cuda", torch.cuda.current_device())
-    peaks, peak_kind = measured_peaks()
+def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
+    """The headline: the decode stack at every batch size, graph-replayed."""
     D, F, n_q, n_kv, hd, tp = QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"]
-    batches = QW["batches"]
+    batches = [int(b) for b in args.batches.split(",")] if args.batches else list(QW["batches"])
     L = args.layers
 
     layers = qwen_stack(L, dev)
@@ -274,7 +271,6 @@ def main():
             forward(B)
 
     # launch list and per-kernel device times (inside a graph, events around each launch)
-    stream = torch.cuda.Stream(device=dev)
     eager_step()
     torch.cuda.synchronize()
     recs = profile_pass(tpl, eager_step, stream)
@@ -365,10 +361,7 @@ def main():
            "oproj": lambda B: D * n_q * hd * 2 + B * n_q * hd * 2}
     roof = None
     if dom in alg:
-        per_b = L  # launches of one tag per forward
-        total_bytes = 0
-        for B in batches:
-            total_bytes += alg[dom](B) * per_b
+        total_bytes = sum(alg[dom](B) * L for B in batches)
         n_launch, t_ms = tot[dom]
         achieved = total_bytes / (t_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -387,50 +380,82 @@ def main():
             agg[tag] = (n + 1, s_ + t)
         per_batch[str(B)]["kernel_us"] = {k: round(v[1] / v[0] * 1e3, 2) for k, v in agg.items()}
         per_batch[str(B)]["sum_kernel_us_per_layer"] = round(sum(v[1] for v in agg.values()) / L * 1e3, 2)
+    out = {"value": value, "ms": ms, "batches": batches, "L": L, "roofline": roof, "e2e": e2e,
+           "gpu_launches": launches_per_step * args.steps, "clocks": clk, "per_batch": per_batch,
+           "kernel_share": share, "layers": layers}
+    return out
 
-    # prefill MLP (Llama-3.1-70B-shaped, TP=8)
+
+def run_prefill(args, tpl, dev, world, peaks, peak_kind, stream):
+    """Llama-3.1-70B-shaped prefill MLP (TP=8), fused shard reduce."""
+    T = args.prefill_tokens
+    P = si.prefill_mlp(T, LP["D"], LP["F"], seed=0, device=dev)
+    Yp = torch.empty((T, LP["D"]), dtype=torch.bfloat16, device=dev)
+    pws = tpl.workspace(tpl.mlp_workspace_bytes(T, LP["D"], LP["F"], LP["tp"]), dev)
+
+    def pstep():
+        tpl.tp_mlp_forward(P["X"], P["Wg"], P["Wu"], P["Wd"], LP["tp"], out=Yp, ws=pws)
+
+    for _ in range(max(3, args.warmup)):
+        pstep()
+    precs = profile_pass(tpl, pstep, stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    psteps = max(5, args.steps // 5)
+    a.record()
+    for _ in range(psteps):
+        pstep()
+    b.record()
+    torch.cuda.synchronize()
+    pms = max_over_ranks(a.elapsed_time(b) / psteps, world)
+    gu = [t for tag, t in precs if tag == "gateup"]
+    dn = [t for tag, t in precs if tag == "down"]
+    gu_flops = 2 * T * LP["D"] * 2 * LP["F"]
+    dn_flops = 2 * T * LP["F"] * LP["D"]
+    flops = gu_flops + dn_flops
+    prefill = {"workload": f"Llama-3.1-70B-shaped prefill MLP X[{T},8192], F=28672, TP=8, fused shard reduce",
+               "value": flops / (pms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": pms,
+               "roofline": {"bound": "tensor", "kernel": "gateup", "achieved": gu_flops / (gu[0] / 1e3) / 1e12,
+                            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": gu_flops / (gu[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
+                            "traffic": None, "peak_kind": peak_kind + " burst"} if gu else None,
+               "down_TFLOP/s": dn_flops / (dn[0] / 1e3) / 1e12 if dn else None,
+               "launches_per_step": len(precs)}
+    del P
+    return prefill
+
+
+def main():
+    args = args_parse()
+    rank, world = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import mlp_megatron_tp_layer_b300 as tpl
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    if args.only == "prefill":
+        pre = run_prefill(args, tpl, dev, world, peaks, peak_kind, stream)
+        if rank == 0:
+            print(json.dumps(dict(pre, metric=METRIC, n_gpus=world, steps=args.steps, warmup=args.warmup)),
+                  flush=True)
+        return
+
+    dec = run_decode(args, tpl, dev, world, peaks, peak_kind, stream)
     prefill = None
-    if not args.no_prefill:
-        P = si.prefill_mlp(LP["B"], LP["D"], LP["F"], seed=0, device=dev)
-        Yp = torch.empty((LP["B"], LP["D"]), dtype=torch.bfloat16, device=dev)
-        pws = tpl.workspace(tpl.mlp_workspace_bytes(LP["B"], LP["D"], LP["F"], LP["tp"]), dev)
-
-        def pstep():
-            tpl.tp_mlp_forward(P["X"], P["Wg"], P["Wu"], P["Wd"], LP["tp"], out=Yp, ws=pws)
-
-        for _ in range(max(3, args.warmup)):
-            pstep()
-        precs = profile_pass(tpl, pstep, stream)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        psteps = max(5, args.steps // 5)
-        a.record()
-        for _ in range(psteps):
-            pstep()
-        b.record()
-        torch.cuda.synchronize()
-        pms = max_over_ranks(a.elapsed_time(b) / psteps, world)
-        gu = [t for tag, t in precs if tag == "gateup"]
-        dn = [t for tag, t in precs if tag == "down"]
-        gu_flops = 2 * LP["B"] * LP["D"] * 2 * LP["F"]
-        dn_flops = 2 * LP["B"] * LP["F"] * LP["D"]
-        prefill = {"workload": "Llama-3.1-70B-shaped prefill MLP X[4096,8192], F=28672, TP=8, fused shard reduce",
-                   "value": PREFILL_FLOPS / (pms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": pms,
-                   "roofline": {"bound": "tensor", "kernel": "gateup", "achieved": gu_flops / (gu[0] / 1e3) / 1e12,
-                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                "frac": gu_flops / (gu[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
-                                "traffic": None, "peak_kind": peak_kind + " burst"} if gu else None,
-                   "down_TFLOP/s": dn_flops / (dn[0] / 1e3) / 1e12 if dn else None,
-                   "launches_per_step": len(precs)}
-        del P
+    if not args.no_prefill and args.only is None:
+        prefill = run_prefill(args, tpl, dev, world, peaks, peak_kind, stream)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(layers, args.cpu_seconds)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only is None:
+        cpu = cpu_baseline(dec["layers"], args.cpu_seconds)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        L, batches = dec["L"], dec["batches"]
+        line = {"metric": METRIC, "value": dec["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": dec["ms"] / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": f"Qwen2.5-1.5B-shaped decode: {L} serial pre-norm layers D=1536 F=8960 "
                                        f"12Q/2KV heads x128, TP=2 logical shards, one forward per B in "
@@ -438,9 +463,9 @@ def main():
                            "global_batch": sum(batches), "parallelism": "tp2 logical shards; 1 replica per GPU",
                            "l2": f"weights {L * QWEN_LAYER_BYTES / 1e9:.2f} GB per forward > 126 MB L2; no flush",
                            "graphs": "one CUDA graph per batch size"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-                "per_batch": per_batch, "kernel_share": share, "prefill": prefill}
+                "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
+                "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
+                "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"], "prefill": prefill}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
