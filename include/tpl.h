@@ -219,8 +219,11 @@ tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, const void* A, 
  * from the calls above (bf16 only):
  *   h = x + Attn(RMSNorm(x));  y = h + MLP(RMSNorm(h))
  * RMSNorm has unit gain and eps = 1e-6 and is computed on every shard
- * ([L4] S4.2: replicated).  Attn and MLP are tp_attn_proj and tp_mlp_forward
- * with the shard reduction fused with the residual add.  x, y [B, D] bf16;
+ * ([L4] S4.2: replicated).  Its per-row scale 1/rms multiplies the fp32
+ * products of the projection that consumes it (RMSNorm(x) W^T =
+ * diag(1/rms(x)) x W^T), so the normalised rows are never rounded to bf16.
+ * Attn and MLP are tp_attn_proj and tp_mlp_forward with the shard reduction
+ * fused with the residual add.  x, y [B, D] bf16;
  * y may equal x.  The stack applies n_layers layers in order; the weight
  * pointer arrays live in HOST memory, one device pointer per layer.
  * This composition goes beyond the pages' four operations; it exists to run

@@ -257,7 +257,7 @@ tpl_status check_mlp_shape(int64_t B, int64_t D, int64_t F, int tp, int dt) {
 
 // Reduce split partials into y (+residual); optionally emit per-shard partials.
 cudaError_t reduce_into(const float* ws, int64_t rows, int64_t cols, const KSplit& ks, float* shard_out,
-                        void* y, int y_bf16, int mode, const void* residual, void* norm_out, unsigned int* rowacc,
+                        void* y, int y_bf16, int mode, const void* residual, float* scale_out, unsigned int* rowacc,
                         cudaStream_t st) {
     ReduceArgs r{};
     r.ws = ws;
@@ -270,39 +270,43 @@ cudaError_t reduce_into(const float* ws, int64_t rows, int64_t cols, const KSpli
     r.y_bf16 = y_bf16;
     r.mode = mode;
     r.residual = residual;
-    r.norm_out = norm_out;
+    r.scale_out = scale_out;
     r.eps = kRmsEps;
     r.ws_up = nullptr;
     r.row_cnt = rowacc;
     r.row_slots = rowacc ? reinterpret_cast<float*>(rowacc + rows) : nullptr;
-    ProfScope prof(norm_out ? "reduce_norm" : "reduce", st);
+    ProfScope prof(scale_out ? "reduce_norm" : "reduce", st);
     return launch_reduce(r, st);
 }
 
-// MLP body shared by tp_mlp_forward and the decoder layer.
+// MLP body shared by tp_mlp_forward and the decoder layer.  Decoder layer
+// only: row_scale (the input's RMSNorm scales, applied to the gate/up
+// products), residual (added to the reduced sum) and scale_out (the output's
+// RMSNorm scales).
 cudaError_t run_mlp(const void* X, const void* Wg, const void* Wu, const void* Wd, void* Y, float* partials,
-                    int64_t B, int64_t D, int64_t F, int tp, int dt, int out_dt, char* ws, const void* residual,
-                    void* norm_out, unsigned int* rowacc, cudaStream_t st) {
+                    int64_t B, int64_t D, int64_t F, int tp, int dt, int out_dt, char* ws, const float* row_scale,
+                    const void* residual, float* scale_out, unsigned int* rowacc, cudaStream_t st) {
     const MlpPlan p = plan_mlp(B, D, F, tp, dt, partials != nullptr);
     void* H = ws + p.h_off;
     const int bf = dt == TPL_BF16;
     const int ybf = out_dt == TPL_BF16;
     Epilogue e{};
     e.mode = EPI_SWIGLU; e.out = H; e.out_bf16 = bf; e.ldo = F;
+    e.row_scale = row_scale;
     cudaError_t err = project("gateup", dt, X, D, B, Wg, Wu, D, F, D, whole(D), e, st);
     if (err != cudaSuccess) return err;
     const Path path = pick_path(dt, B);
     if (p.fused_tc) {
         // Shard partials accumulate in TMEM in ascending shard order (the K
         // blocks of shard 0 first): the reduction happens inside the GEMM.
-        if (!residual && !norm_out)
+        if (!residual && !scale_out)
             return project("down", dt, H, F, B, Wd, nullptr, F, D, F, whole(F), epi_store(Y, ybf, D), st);
         // decoder layer: the fused sum goes through one fp32 plane so the
         // residual add and the next RMSNorm can follow
         float* sum = reinterpret_cast<float*>(ws + p.part_off);
         err = project("down", dt, H, F, B, Wd, nullptr, F, D, F, whole(F), epi_partial(sum, D, B * D, rowacc, B), st);
         if (err != cudaSuccess) return err;
-        return reduce_into(sum, B, D, whole(D), nullptr, Y, ybf, TPL_ALLREDUCE, residual, norm_out, rowacc, st);
+        return reduce_into(sum, B, D, whole(D), nullptr, Y, ybf, TPL_ALLREDUCE, residual, scale_out, rowacc, st);
     }
     if (path == PATH_TC && partials && p.ks.sub == 1 && tc_split_ok(p.ks)) {
         err = project("down", dt, H, F, B, Wd, nullptr, F, D, F, p.ks, epi_partial(partials, D, B * D, rowacc, B),
@@ -310,12 +314,12 @@ cudaError_t run_mlp(const void* X, const void* Wg, const void* Wu, const void* W
         if (err != cudaSuccess) return err;
         KSplit one = p.ks;
         one.sub = 1;
-        return reduce_into(partials, B, D, one, nullptr, Y, ybf, TPL_ALLREDUCE, residual, norm_out, rowacc, st);
+        return reduce_into(partials, B, D, one, nullptr, Y, ybf, TPL_ALLREDUCE, residual, scale_out, rowacc, st);
     }
     float* part = reinterpret_cast<float*>(ws + p.part_off);
     err = project("down", dt, H, F, B, Wd, nullptr, F, D, F, p.ks, epi_partial(part, D, B * D, rowacc, B), st);
     if (err != cudaSuccess) return err;
-    return reduce_into(part, B, D, p.ks, partials, Y, ybf, TPL_ALLREDUCE, residual, norm_out, rowacc, st);
+    return reduce_into(part, B, D, p.ks, partials, Y, ybf, TPL_ALLREDUCE, residual, scale_out, rowacc, st);
 }
 
 // ------------------------------------------------- attention projections
@@ -352,9 +356,11 @@ AttnPlan plan_attn(int64_t B, int64_t D, int n_q, int n_kv, int hd, int tp, int 
     return p;
 }
 
+// Decoder-layer arguments as in run_mlp (row_scale applies to the QKV products).
 cudaError_t run_attn(const void* X, const void* Wqkv, const void* Wo, void* qkv_out, void* Y, float* partials,
                      int64_t B, int64_t D, int n_q, int n_kv, int hd, int tp, int dt, int out_dt, char* ws,
-                     const void* residual, void* norm_out, unsigned int* rowacc, cudaStream_t st) {
+                     const float* row_scale, const void* residual, float* scale_out, unsigned int* rowacc,
+                     cudaStream_t st) {
     const AttnPlan p = plan_attn(B, D, n_q, n_kv, hd, tp, dt);
     const int bf = dt == TPL_BF16;
     void* qkv = qkv_out ? qkv_out : ws + p.qkv_off;
@@ -366,27 +372,29 @@ cudaError_t run_attn(const void* X, const void* Wqkv, const void* Wo, void* qkv_
     e.qkv.nq_s = p.nq_s; e.qkv.kv_s = p.kv_s;
     e.qkv.w_s = p.w_s; e.qkv.shard_stride = B * p.w_s;
     e.qkv.qkv_out = qkv; e.qkv.o_out = O; e.qkv.ldo_o = (int64_t)n_q * hd;
+    e.row_scale = row_scale;
     cudaError_t err = project("qkv", dt, X, D, B, Wqkv, nullptr, D, p.nqkv, D, whole(D), e, st);
     if (err != cudaSuccess) return err;
     const int64_t K = (int64_t)n_q * hd;
     float* part = reinterpret_cast<float*>(ws + p.part_off);
     err = project("oproj", dt, O, K, B, Wo, nullptr, K, D, K, p.ks, epi_partial(part, D, B * D, rowacc, B), st);
     if (err != cudaSuccess) return err;
-    return reduce_into(part, B, D, p.ks, partials, Y, out_dt == TPL_BF16, TPL_ALLREDUCE, residual, norm_out, rowacc,
-                       st);
+    return reduce_into(part, B, D, p.ks, partials, Y, out_dt == TPL_BF16, TPL_ALLREDUCE, residual, scale_out,
+                       rowacc, st);
 }
 
 // ------------------------------------------------------- decoder layer
 struct LayerPlan {
-    size_t xn_off, h_off, hn_off, acc_off, attn_off, mlp_off, total;
+    size_t sx_off, h_off, sh_off, acc_off, attn_off, mlp_off, total;
 };
 LayerPlan plan_layer(int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int hd, int tp) {
     LayerPlan p{};
     const size_t act = up((size_t)B * D * 2);
-    p.xn_off = 0;
-    p.h_off = act;
-    p.hn_off = 2 * act;
-    p.acc_off = 3 * act;                            // row accumulators of the norm reductions
+    const size_t scl = up((size_t)B * 4);
+    p.sx_off = 0;                                   // RMSNorm scales of the layer input
+    p.h_off = scl;
+    p.sh_off = scl + act;                           // RMSNorm scales of h
+    p.acc_off = 2 * scl + act;                      // row accumulators of the norm reductions
     p.attn_off = p.acc_off + up(rowacc_bytes(B, D));
     const size_t attn = plan_attn(B, D, n_q, n_kv, hd, tp, TPL_BF16).total;
     p.mlp_off = p.attn_off + up(attn);
@@ -396,24 +404,24 @@ LayerPlan plan_layer(int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int hd,
 
 cudaError_t run_layer(const void* x, void* y, const void* Wqkv, const void* Wo, const void* Wg, const void* Wu,
                       const void* Wd, int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int hd, int tp,
-                      char* ws, bool x_normed_ready, cudaStream_t st) {
+                      char* ws, bool x_scale_ready, cudaStream_t st) {
     const LayerPlan p = plan_layer(B, D, F, n_q, n_kv, hd, tp);
-    void* xn = ws + p.xn_off;
+    float* sx = reinterpret_cast<float*>(ws + p.sx_off);
     void* h = ws + p.h_off;
-    void* hn = ws + p.hn_off;
+    float* sh = reinterpret_cast<float*>(ws + p.sh_off);
     unsigned int* rowacc = reinterpret_cast<unsigned int*>(ws + p.acc_off);
     cudaError_t err;
-    if (!x_normed_ready) {
+    if (!x_scale_ready) {
         ProfScope prof("rmsnorm", st);
-        err = launch_rmsnorm(x, xn, B, D, kRmsEps, rowacc, st);
+        err = launch_rmsnorm(x, sx, B, D, kRmsEps, rowacc, st);
         if (err != cudaSuccess) return err;
     }
-    // attention sublayer: h = x + sum_s P_s, hn = RMSNorm(h)
-    err = run_attn(xn, Wqkv, Wo, nullptr, h, nullptr, B, D, n_q, n_kv, hd, tp, TPL_BF16, TPL_BF16, ws + p.attn_off, x,
-                   hn, rowacc, st);
+    // attention sublayer on RMSNorm(x) = diag(sx) x: h = x + sum_s P_s, and h's scales
+    err = run_attn(x, Wqkv, Wo, nullptr, h, nullptr, B, D, n_q, n_kv, hd, tp, TPL_BF16, TPL_BF16, ws + p.attn_off, sx,
+                   x, sh, rowacc, st);
     if (err != cudaSuccess) return err;
-    // MLP sublayer: y = h + sum_s P_s, and the next layer's RMSNorm(y) into xn
-    return run_mlp(hn, Wg, Wu, Wd, y, nullptr, B, D, F, tp, TPL_BF16, TPL_BF16, ws + p.mlp_off, h, xn, rowacc, st);
+    // MLP sublayer on RMSNorm(h): y = h + sum_s P_s, and y's scales (the next layer's sx)
+    return run_mlp(h, Wg, Wu, Wd, y, nullptr, B, D, F, tp, TPL_BF16, TPL_BF16, ws + p.mlp_off, sh, h, sx, rowacc, st);
 }
 
 }  // namespace
@@ -503,7 +511,7 @@ extern "C" tpl_status tpl_tp_mlp_forward(const void* X, const void* Wg, const vo
     if (overlap(ws, need, X, (size_t)B * D * es) || overlap(ws, need, Y, ybytes)) return TPL_ERR_ALIAS;
     if (!device_ctx()) return TPL_ERR_CUDA;
     return cuda_status(run_mlp(X, Wg, Wu, Wd, Y, partials, B, D, F, tp, dtype, out_dtype, static_cast<char*>(ws),
-                               nullptr, nullptr, nullptr, S(stream)));
+                               nullptr, nullptr, nullptr, nullptr, S(stream)));
 }
 
 extern "C" tpl_status tpl_tp_attn_proj_workspace(int64_t B, int64_t D, int n_q, int n_kv, int head_dim, int tp,
@@ -538,7 +546,7 @@ extern "C" tpl_status tpl_tp_attn_proj(const void* X, const void* Wqkv, const vo
     if (overlap(ws, p.total, X, (size_t)B * D * es) || overlap(ws, p.total, Y, ybytes)) return TPL_ERR_ALIAS;
     if (!device_ctx()) return TPL_ERR_CUDA;
     return cuda_status(run_attn(X, Wqkv, Wo, qkv_out, Y, partials, B, D, n_q, n_kv, head_dim, tp, dtype, out_dtype,
-                                static_cast<char*>(ws), nullptr, nullptr, nullptr, S(stream)));
+                                static_cast<char*>(ws), nullptr, nullptr, nullptr, nullptr, S(stream)));
 }
 
 // ------------------------------------------------------------ four cases
@@ -696,8 +704,8 @@ extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* c
     if (!device_ctx()) return TPL_ERR_CUDA;
     cudaStream_t st = S(stream);
     for (int l = 0; l < n_layers; ++l) {
-        // every layer after the first finds RMSNorm(x) already produced by
-        // the previous layer's final reduction
+        // every layer after the first finds the RMSNorm scales of its input
+        // already produced by the previous layer's final reduction
         cudaError_t e = run_layer(l == 0 ? x : y, y, Wqkv[l], Wo[l], Wg[l], Wu[l], Wd[l], B, D, F, n_q, n_kv,
                                   head_dim, tp, static_cast<char*>(ws), l > 0, st);
         if (e != cudaSuccess) return TPL_ERR_CUDA;

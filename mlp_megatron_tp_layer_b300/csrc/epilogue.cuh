@@ -64,7 +64,7 @@ __device__ __forceinline__ void store_value(const Epilogue& e, int split, int64_
         e.out32[(int64_t)split * e.split_stride + t * e.ldo + f] = v;
         break;
     case EPI_QKV:
-        store_qkv(e.qkv, t, f, v, e.out_bf16);
+        store_qkv(e.qkv, t, f, e.row_scale ? v * e.row_scale[t] : v, e.out_bf16);
         break;
     default:
         break;
@@ -73,6 +73,11 @@ __device__ __forceinline__ void store_value(const Epilogue& e, int split, int64_
 
 __device__ __forceinline__ void store_pair(const Epilogue& e, int split, int64_t t, int64_t f, float g, float u) {
     if (e.mode == EPI_SWIGLU) {
+        if (e.row_scale) {
+            const float s = e.row_scale[t];
+            g *= s;
+            u *= s;
+        }
         put(e.out, t * e.ldo + f, silu_f(g) * u, e.out_bf16);
     } else {  // EPI_PARTIAL2
         const int64_t off = (int64_t)split * e.split_stride + t * e.ldo + f;

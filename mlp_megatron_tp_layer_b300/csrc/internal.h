@@ -42,6 +42,8 @@ struct Epilogue {
     int64_t block_stride;
     int64_t split_stride;  // EPI_PARTIAL(2): elements between split planes
     QkvMap qkv;
+    const float* row_scale;    // EPI_QKV / EPI_SWIGLU: per-token factor applied to the fp32 products
+                               // (the folded RMSNorm scale 1/rms), or null
     unsigned int* zero_words;  // if set, block 0 of the launch zeroes zero_count words at start
     int zero_count;            // (row accumulators of the reduction that consumes this output)
 };
@@ -85,7 +87,8 @@ cudaError_t launch_rowdot(const RowdotArgs& a, bool bf16, cudaStream_t st);
 // chunks, then over shards in ascending order.  Optional outputs: the shard
 // partials [tp, rows, cols] fp32, and y = residual + sum written as dtype
 // (layout ALLREDUCE [rows, cols] or REDUCE_SCATTER [tp, rows, cols/tp]).
-// Optional norm_out = RMSNorm(bf16(y)) (bf16), which needs the whole row.
+// Optional scale_out[row] = 1 / sqrt(mean(bf16(y)^2) + eps), the RMSNorm
+// scale of each row, which needs the whole row.
 struct ReduceArgs {
     const float* ws;
     int64_t rows, cols;
@@ -95,11 +98,11 @@ struct ReduceArgs {
     int y_bf16;
     int mode;              // tpl_reduce_mode
     const void* residual;  // bf16 [rows, cols] or null
-    void* norm_out;        // bf16 [rows, cols] or null
+    float* scale_out;      // [rows] RMSNorm scales, or null
     float eps;
     const float* ws_up;    // non-null: ws/ws_up are gate/up planes -> y = silu(sum ws) * sum ws_up
-    unsigned int* row_cnt; // norm_out only: [rows] block tickets, zero on entry (reset on exit)
-    float* row_slots;      // norm_out only: [rows, norm_blocks(cols)] per-block sums of squares
+    unsigned int* row_cnt; // scale_out only: [rows] block tickets, zero on entry (reset on exit)
+    float* row_slots;      // scale_out only: [rows, norm_blocks(cols)] per-block sums of squares
 };
 
 // The row-normalising reduction covers kNormCols columns per block; a row's
@@ -110,9 +113,10 @@ inline int64_t norm_blocks(int64_t cols) { return (cols + kNormCols - 1) / kNorm
 inline size_t rowacc_bytes(int64_t rows, int64_t cols) { return (size_t)rows * 4 * (1 + norm_blocks(cols)); }
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st);
 
-// RMSNorm of bf16 rows (unit gain); zeroes the tickets of rowacc itself.
-cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, unsigned int* rowacc,
-                           cudaStream_t st);
+// RMSNorm scales of bf16 rows: scale[r] = 1 / sqrt(mean(x[r]^2) + eps) (unit
+// gain); zeroes the tickets of rowacc itself.
+cudaError_t launch_rmsnorm(const void* x, float* scale, int64_t rows, int64_t cols, float eps,
+                           unsigned int* rowacc, cudaStream_t st);
 
 // ---------------------------------------------------- tensor-core GEMM
 // D[M, N] = A[M, K] B[N, K]^T, A and B bf16 K-major.  `swap` means A holds the

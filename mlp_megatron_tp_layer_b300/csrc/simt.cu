@@ -237,8 +237,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // partials) for its kNormCols columns (or y = x when tp == 0), and its share of
 // the row's sum of squares of the ROUNDED values, written to its own slot.  The
 // last block of a row to finish (atomic ticket; nothing waits) adds the slots
-// in block order -- the same sum whatever order the blocks ran in -- and
-// scales the whole row: norm_out = bf16(y / sqrt(mean(y^2) + eps)).  row_cnt
+// in block order -- the same sum whatever order the blocks ran in -- and writes
+// the row's RMSNorm scale: scale_out = 1 / sqrt(mean(y^2) + eps).  row_cnt
 // starts at zero (the kernel that produced the partials zeroes it) and the
 // last block resets it.
 __global__ void __launch_bounds__(kNormThreads) reduce_norm_kernel(const ReduceArgs a) {
@@ -287,24 +287,12 @@ __global__ void __launch_bounds__(kNormThreads) reduce_norm_kernel(const ReduceA
     if (ticket != gridDim.x - 1) return;
     // last block of this row: every other block's y and slot are visible
     __threadfence();
-    float total = 0.f;
-    for (unsigned b = 0; b < gridDim.x; ++b) total += __ldcg(slots + b);
-    const float scale = 1.0f / sqrtf(total / (float)a.cols + a.eps);
-    const __nv_bfloat16* src = y ? y : res;     // y == null only for the plain RMSNorm (tp == 0)
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.norm_out);
-    for (int64_t cc = (int64_t)threadIdx.x * 4; cc < a.cols; cc += kNormThreads * 4) {
-        const int64_t i = row * a.cols + cc;
-        const uint2 rv = __ldcg(reinterpret_cast<const uint2*>(src + i));
-        const float f[4] = {__uint_as_float(rv.x << 16), __uint_as_float(rv.x & 0xFFFF0000u),
-                            __uint_as_float(rv.y << 16), __uint_as_float(rv.y & 0xFFFF0000u)};
-        uint2 w;
-        w.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[0] * scale)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[1] * scale)) << 16);
-        w.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[2] * scale)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f[3] * scale)) << 16);
-        *reinterpret_cast<uint2*>(out + i) = w;
+    if (threadIdx.x == 0) {
+        float total = 0.f;
+        for (unsigned b = 0; b < gridDim.x; ++b) total += __ldcg(slots + b);
+        a.scale_out[row] = 1.0f / sqrtf(total / (float)a.cols + a.eps);
+        a.row_cnt[row] = 0u;
     }
-    if (threadIdx.x == 0) a.row_cnt[row] = 0u;
 }
 
 // Zero the row accumulators before a plain RMSNorm (no producing GEMM precedes it).
@@ -322,7 +310,7 @@ cudaError_t launch_rowdot(const RowdotArgs& a, bool bf16, cudaStream_t st) {
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
-    if (a.norm_out) {
+    if (a.scale_out) {
         dim3 grid((unsigned)norm_blocks(a.cols), (unsigned)a.rows);
         reduce_norm_kernel<<<grid, kNormThreads, 0, st>>>(a);
         return cudaGetLastError();
@@ -335,8 +323,8 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, float eps, unsigned int* rowacc,
-                           cudaStream_t st) {
+cudaError_t launch_rmsnorm(const void* x, float* scale, int64_t rows, int64_t cols, float eps,
+                           unsigned int* rowacc, cudaStream_t st) {
     zero_words_kernel<<<1, 256, 0, st>>>(rowacc, (int)rows);
     ReduceArgs a{};
     a.ws = nullptr;
@@ -346,7 +334,7 @@ cudaError_t launch_rmsnorm(const void* x, void* y, int64_t rows, int64_t cols, f
     a.sub = 1;
     a.residual = x;
     a.y = nullptr;
-    a.norm_out = y;
+    a.scale_out = scale;
     a.eps = eps;
     a.row_cnt = rowacc;
     a.row_slots = reinterpret_cast<float*>(rowacc + rows);

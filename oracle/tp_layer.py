@@ -31,8 +31,10 @@ Readings where the pages are silent (each also listed in the design doc):
     single-device results differ only by the order of that sum).
   * bf16 rounding (round-to-nearest-even) happens exactly where the CUDA path
     stores a bf16 tensor: the SwiGLU output H, the packed QKV output, the
-    RMSNorm outputs, the residual stream and every bf16 result.  Partials stay
-    unrounded.
+    residual stream and every bf16 result.  Partials stay unrounded.  The
+    RMSNorm output is not stored: its per-row scale 1/rms multiplies the
+    consuming projection's products, RMSNorm(x) W^T = diag(1/rms(x)) (x W^T),
+    so the normalised activations are never rounded to bf16.
   * A tensor sharded along its last dimension, e.g. C[I, K_X], is stored as the
     concatenation of the device-local shards: [X, I, K/X].  One sharded along
     its first dimension, C[I_X, K], is then simply [I, K] row-major.
@@ -378,14 +380,14 @@ def decoder_layer(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, shard
     If ``trace`` is a list, the two rounded residual-stream values h and y are
     appended to it (read-only instrumentation; the arithmetic is unchanged).
     """
-    xn = bf16_round(rmsnorm(x))
+    xn = rmsnorm(x)          # not rounded: its scale is applied to the products
     if sharded:
         a, _, _, P = attn_proj_sharded(xn, W["Wqkv"], W["Wo"], n_q, n_kv, head_dim, tp)
         a_sum = shard_reduce(P, False)
     else:
         a_sum = linear_attn_sum(xn, W, n_q, n_kv, head_dim)
     h = bf16_round(_f64(x) + a_sum)
-    hn = bf16_round(rmsnorm(h))
+    hn = rmsnorm(h)
     if sharded:
         _, P, _ = mlp_sharded(hn, W["Wg"], W["Wu"], W["Wd"], tp, bf16=True)
         m_sum = shard_reduce(P, False)

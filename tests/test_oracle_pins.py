@@ -376,7 +376,7 @@ def test_decoder_layer_zero_output_projections_is_identity():
     # with only the MLP silenced the layer adds the attention sublayer once
     W["Wo"] = r.standard_normal((D, n_q * hd)) / 8
     y = O.decoder_layer(x, W, n_q, n_kv, hd, tp=2)
-    a, _ = O.attn_proj_unsharded(O.bf16_round(O.rmsnorm(x)), W["Wqkv"], W["Wo"], n_q, n_kv, hd, bf16=False)
+    a, _ = O.attn_proj_unsharded(O.rmsnorm(x), W["Wqkv"], W["Wo"], n_q, n_kv, hd, bf16=False)
     assert np.allclose(y, O.bf16_round(x + a), rtol=0, atol=2 ** -7 * np.abs(x + a).max())
 
 
