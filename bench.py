@@ -355,13 +355,17 @@ def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
         n, s = tot.get(tag, (0, 0.0))
         tot[tag] = (n + 1, s + t)
     dom = max(tot, key=lambda k: tot[k][1])
-    alg = {"gateup": lambda B: 2 * F * D * 2 + B * D * 2 + B * F * 2,
-           "down": lambda B: D * F * 2 + B * F * 2 + B * D * 4 * 0,
-           "qkv": lambda B: (n_q + 2 * n_kv) * hd * D * 2 + B * D * 2,
-           "oproj": lambda B: D * n_q * hd * 2 + B * n_q * hd * 2}
+    # algorithmic bytes of one launch of each step: the weights it must stream
+    # once plus its activation input and output (per-layer steps launch L times
+    # per forward, the fused stack once per forward for all L layers)
+    alg = {"gateup": lambda B: L * (2 * F * D * 2 + B * D * 2 + B * F * 2),
+           "down": lambda B: L * (D * F * 2 + B * F * 2 + B * D * 4),
+           "qkv": lambda B: L * ((n_q + 2 * n_kv) * hd * D * 2 + B * D * 2),
+           "oproj": lambda B: L * (D * n_q * hd * 2 + B * n_q * hd * 2),
+           "fused_stack": lambda B: L * QWEN_LAYER_BYTES + 2 * B * D * 2}
     roof = None
     if dom in alg:
-        total_bytes = sum(alg[dom](B) * L for B in batches)
+        total_bytes = sum(alg[dom](B) for B in batches)
         n_launch, t_ms = tot[dom]
         achieved = total_bytes / (t_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -228,7 +228,21 @@ tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, const void* A, 
  * pointer arrays live in HOST memory, one device pointer per layer.
  * This composition goes beyond the pages' four operations; it exists to run
  * a whole decode step.
+ *
+ * Two implementations compute it.  FUSED (B <= 128 tokens; D, F and
+ * n_q head_dim multiples of 64): one persistent cooperative launch per up to
+ * 32 layers streams every weight once through tensor-core GEMMs with the
+ * weights as the M operand; split-K partial tiles are added by the last CTA
+ * to finish each tile, in k (shard) order.  UNFUSED: one launch per
+ * projection and per shard reduction.  The two add partial sums in
+ * different orders, so they agree to rounding, not bit for bit; each is
+ * deterministic.  tpl_tp_decoder_stack / _layer take FUSED where it applies.
  * ------------------------------------------------------------------------ */
+typedef enum tpl_decode_path {
+    TPL_PATH_AUTO = 0,      /* FUSED where it applies, else UNFUSED */
+    TPL_PATH_UNFUSED = 1,
+    TPL_PATH_FUSED = 2      /* TPL_ERR_UNSUPPORTED where it does not apply */
+} tpl_decode_path;
 tpl_status tpl_tp_decoder_workspace(int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
                                     int head_dim, int tp, size_t* bytes);
 tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* Wqkv, const void* Wo,
@@ -240,6 +254,13 @@ tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv,
                                 const void* const* Wu, const void* const* Wd, int n_layers,
                                 int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int head_dim,
                                 int tp, void* ws, size_t ws_bytes, void* stream);
+/* tp_decoder_stack with the implementation chosen by `path` (tpl_decode_path). */
+tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
+                                     const void* const* Wo, const void* const* Wg,
+                                     const void* const* Wu, const void* const* Wd, int n_layers,
+                                     int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
+                                     int head_dim, int tp, void* ws, size_t ws_bytes, int path,
+                                     void* stream);
 
 /* --------------------------------------------------------------------------
  * Launch timing, for measurement only (off by default).

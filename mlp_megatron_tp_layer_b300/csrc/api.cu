@@ -24,7 +24,6 @@ namespace {
 
 constexpr int kSimtMaxTokens = 8;     // tokens per row-dot launch
 constexpr int kDesignSMs = 148;       // split-K sizing target (B300); shapes only, so queries match launches
-constexpr float kRmsEps = 1e-6f;
 constexpr size_t kAlign = 256;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -271,7 +270,7 @@ cudaError_t reduce_into(const float* ws, int64_t rows, int64_t cols, const KSpli
     r.mode = mode;
     r.residual = residual;
     r.scale_out = scale_out;
-    r.eps = kRmsEps;
+    r.eps = kRmsEpsilon;
     r.ws_up = nullptr;
     r.row_cnt = rowacc;
     r.row_slots = rowacc ? reinterpret_cast<float*>(rowacc + rows) : nullptr;
@@ -413,7 +412,7 @@ cudaError_t run_layer(const void* x, void* y, const void* Wqkv, const void* Wo, 
     cudaError_t err;
     if (!x_scale_ready) {
         ProfScope prof("rmsnorm", st);
-        err = launch_rmsnorm(x, sx, B, D, kRmsEps, rowacc, st);
+        err = launch_rmsnorm(x, sx, B, D, kRmsEpsilon, rowacc, st);
         if (err != cudaSuccess) return err;
     }
     // attention sublayer on RMSNorm(x) = diag(sx) x: h = x + sum_s P_s, and h's scales
@@ -671,7 +670,10 @@ extern "C" tpl_status tpl_tp_decoder_workspace(int64_t B, int64_t D, int64_t F, 
     if (s != TPL_OK) return s;
     s = check_attn_shape(B, D, n_q, n_kv, head_dim, tp, TPL_BF16);
     if (s != TPL_OK) return s;
-    *bytes = plan_layer(B, D, F, n_q, n_kv, head_dim, tp).total;
+    size_t need = plan_layer(B, D, F, n_q, n_kv, head_dim, tp).total;
+    const FusedShape fs{B, D, F, n_q, n_kv, head_dim, tp};
+    if (fused_stack_shape_ok(fs)) need = std::max(need, fused_stack_ws_bytes(fs));
+    *bytes = need;
     return TPL_OK;
 }
 
@@ -683,11 +685,13 @@ static tpl_status check_layer_args(const void* x, const void* y, const void* Wqk
     return TPL_OK;
 }
 
-extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv, const void* const* Wo,
-                                           const void* const* Wg, const void* const* Wu, const void* const* Wd,
-                                           int n_layers, int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
-                                           int head_dim, int tp, void* ws, size_t ws_bytes, void* stream) {
+extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
+                                                const void* const* Wo, const void* const* Wg, const void* const* Wu,
+                                                const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,
+                                                int n_q, int n_kv, int head_dim, int tp, void* ws, size_t ws_bytes,
+                                                int path, void* stream) {
     if (!Wqkv || !Wo || !Wg || !Wu || !Wd || !ws) return TPL_ERR_NULL;
+    if (path != TPL_PATH_AUTO && path != TPL_PATH_UNFUSED && path != TPL_PATH_FUSED) return TPL_ERR_UNSUPPORTED;
     if (n_layers <= 0) return TPL_ERR_SHAPE;
     size_t need = 0;
     tpl_status s = tpl_tp_decoder_workspace(B, D, F, n_q, n_kv, head_dim, tp, &need);
@@ -703,6 +707,13 @@ extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* c
     if (x != y && overlap(x, act, y, act)) return TPL_ERR_ALIAS;
     if (!device_ctx()) return TPL_ERR_CUDA;
     cudaStream_t st = S(stream);
+    const FusedShape fs{B, D, F, n_q, n_kv, head_dim, tp};
+    const bool fused_ok = fused_stack_shape_ok(fs) && tc_gemm_supported();
+    if (path == TPL_PATH_FUSED && !fused_ok) return TPL_ERR_UNSUPPORTED;
+    if (path != TPL_PATH_UNFUSED && fused_ok) {
+        ProfScope prof("fused_stack", st);
+        return cuda_status(launch_fused_stack(fs, x, y, Wqkv, Wo, Wg, Wu, Wd, n_layers, ws, st));
+    }
     for (int l = 0; l < n_layers; ++l) {
         // every layer after the first finds the RMSNorm scales of its input
         // already produced by the previous layer's final reduction
@@ -711,6 +722,14 @@ extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* c
         if (e != cudaSuccess) return TPL_ERR_CUDA;
     }
     return TPL_OK;
+}
+
+extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv, const void* const* Wo,
+                                           const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                                           int n_layers, int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
+                                           int head_dim, int tp, void* ws, size_t ws_bytes, void* stream) {
+    return tpl_tp_decoder_stack_path(x, y, Wqkv, Wo, Wg, Wu, Wd, n_layers, B, D, F, n_q, n_kv, head_dim, tp, ws,
+                                     ws_bytes, TPL_PATH_AUTO, stream);
 }
 
 extern "C" tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* Wqkv, const void* Wo, const void* Wg,

@@ -1,0 +1,893 @@
+// Fused decode stack: ONE persistent launch runs every layer of a serial
+// pre-norm decoder stack (h = x + Attn(RMSNorm(x)); y = h + MLP(RMSNorm(h)))
+// for a small batch of tokens (B <= 128), with the tensor-parallel shards as
+// logical weight partitions.
+//
+// Each layer is four projections, each a "phase" of the launch:
+//   QKV    [n_qkv, D] . RMSNorm(x)      -> packed QKV (shard blocks) and the
+//                                          context-1 attention output O
+//   OPROJ  [D, n_q hd] . O  (row-par.)  -> h = x + sum over shards
+//   GATEUP [F, D] x2 . RMSNorm(h)       -> H = silu(gate) * up
+//   DOWN   [D, F] . H       (row-par.)  -> y = h + sum over shards
+// Weights are the M = 128 operand of tcgen05.mma (kind::f16), tokens the N
+// operand (padded to NP by TMA's zero fill), accumulators in TMEM.
+//
+// Work split: a phase's work is the flattened list of (m-tile, 64-wide
+// k-block) pairs; CTA c of G takes the contiguous range [c T/G, (c+1) T/G).
+// A range may cover parts of several m-tiles ("units"); each unit leaves an
+// fp32 partial tile in global memory and counts itself on the tile's ticket.
+// Once all of a tile's units have arrived, the CTAs that hold them each
+// finalize a share of the tile's tokens: they add the tile's partials in k
+// order (the order of the shards for the row-parallel phases) and apply the
+// phase's epilogue.  The sum is therefore the same whatever order the CTAs
+// ran in.
+//
+// Phases are separated by a grid barrier: one counter in global memory that
+// every CTA increments when it has finished a phase, and only after the
+// barrier of that phase has passed, so that it reaching G (k+1) means phases
+// 0..k are complete everywhere.  The launch is cooperative, so every CTA is
+// resident and these waits (all bounded in time) can be met.  Weight tiles do
+// not depend on the activations, so the weight producer keeps loading the
+// next phase's weights into the shared-memory ring, and prefetching further
+// ones into L2, while the barrier is pending; only the activation loads wait
+// for it.
+//
+// RMSNorm: the producer of a residual-stream value also writes, per 128-column
+// tile and token, the sum of squares of the rounded values; the consumer's
+// epilogue turns the tile sums into 1/rms and multiplies its fp32 products by
+// it (RMSNorm(x) W^T = diag(1/rms(x)) x W^T).
+//
+// Warp roles (256 threads): 0 weight TMA producer, 1 TMEM owner + MMA issuer,
+// 2..5 epilogue (warp w reads TMEM lanes 32 (w % 4) ..), 6 activation TMA
+// producer, 7 L2 prefetch of the weights ahead of the MMA.  Every wait is bounded in time; on expiry the CTA sets the grid
+// abort flag and the sticky device error word, and every role winds down.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpl {
+namespace {
+
+constexpr int kFThreads = 256;
+constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6, kWarpPf = 7;
+constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
+constexpr int kAccStride = 256;
+constexpr int kL2Ahead = 32;       // weight tiles prefetched into L2 ahead of the MMA
+enum Kind { K_QKV = 0, K_OPROJ = 1, K_GATEUP = 2, K_DOWN = 3 };
+enum ActMap { A_X = 0, A_R0 = 1, A_R1 = 2, A_O = 3, A_H = 4, A_HID = 5, A_COUNT = 6 };
+enum WMap { W_QKV = 0, W_O = 1, W_G = 2, W_U = 3, W_D = 4, W_COUNT = 5 };
+
+// Tensor maps travel as a __grid_constant__ kernel parameter (about 21 KB).
+struct FusedMaps {
+    CUtensorMap act[A_COUNT];                      // [B rows, cols] bf16, box NP x 64
+    CUtensorMap w[kFusedMaxLayers][W_COUNT];       // [rows, K] bf16, box 128 x 64
+};
+
+struct FusedParams {
+    int B, D, F, L, G;
+    int n_qkv, ko;             // packed QKV rows, o_proj input width n_q hd
+    int max_mt;                // ticket row length
+    float eps;
+    QkvMap qkv;                // packed-QKV scatter (qkv_out = shard blocks, o_out = O)
+    const __nv_bfloat16* x_in;
+    __nv_bfloat16 *y_out, *R0, *R1, *O, *h, *H;
+    float* slots_y;            // [ceil(D/128)][B] sums of squares of the layer input / output
+    float* slots_h;            // [ceil(D/128)][B] sums of squares of h
+    float* part;               // partial tiles, [G + max_mt][2][NP][128] fp32
+    unsigned* tickets;         // [4][max_mt]
+    unsigned* bar;             // grid barrier counter (zero at launch)
+    int* gabort;               // grid abort flag (zero at launch)
+    unsigned* err;
+    const __nv_bfloat16* wptr[kFusedMaxLayers][W_COUNT];   // weight bases (for L2 prefetch)
+};
+
+template <int NP>
+struct FCfg {
+    static constexpr int W_BYTES = 128 * 64 * 2;                 // one 128 x 64 weight tile
+    static constexpr int X_BYTES = NP * 64 * 2;                  // the NP x 64 activation tile
+    static constexpr int STAGE = W_BYTES + X_BYTES;
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr int CTRL = 1024;                            // mbarriers and flags
+    static constexpr int EPI = 128 * 4 + (kFusedGridCap + 4) * 4;   // RMSNorm scales, segment list
+    static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI;
+    static constexpr int PART_FLOATS = 2 * NP * 128;             // one partial slot
+    static constexpr int CH = NP >= 32 ? 32 : 16;                // TMEM columns per load
+    static_assert(NP % 16 == 0 && NP >= 16 && NP <= 128, "N of an M=128 MMA: 16..256, step 16");
+    static_assert(STAGE % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
+    static_assert(3 * STAGES + 5 <= 120, "mbarriers must fit the control block");
+};
+
+struct Phase {
+    int kind, layer, m_tiles, nkb, M, K;
+    int64_t total;
+    const __nv_bfloat16* pa;
+    const __nv_bfloat16* pb;
+    const CUtensorMap* wa;
+    const CUtensorMap* wb;
+    const CUtensorMap* act;
+};
+
+// Phase k >= 1 of the launch: layer (k-1)/4, projection (k-1)%4.
+__device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams& p, int k) {
+    Phase ph;
+    ph.layer = (k - 1) >> 2;
+    ph.kind = (k - 1) & 3;
+    const int l = ph.layer;
+    int K, wa, wb = -1;
+    switch (ph.kind) {
+    case K_QKV:
+        ph.M = p.n_qkv; K = p.D; wa = W_QKV;
+        ph.act = &mp.act[l == 0 ? A_X : (((l - 1) & 1) ? A_R1 : A_R0)];
+        break;
+    case K_OPROJ:
+        ph.M = p.D; K = p.ko; wa = W_O; ph.act = &mp.act[A_O];
+        break;
+    case K_GATEUP:
+        ph.M = p.F; K = p.D; wa = W_G; wb = W_U; ph.act = &mp.act[A_H];
+        break;
+    default:
+        ph.M = p.D; K = p.F; wa = W_D; ph.act = &mp.act[A_HID];
+        break;
+    }
+    ph.wa = &mp.w[l][wa];
+    ph.wb = wb < 0 ? nullptr : &mp.w[l][wb];
+    ph.pa = p.wptr[l][wa];
+    ph.pb = wb < 0 ? nullptr : p.wptr[l][wb];
+    ph.K = K;
+    ph.m_tiles = (ph.M + 127) / 128;
+    ph.nkb = (K + 63) / 64;
+    ph.total = (int64_t)ph.m_tiles * ph.nkb;
+    return ph;
+}
+
+// The CTA owning flattened index a: the largest c with floor(c T / G) <= a.
+__device__ __forceinline__ int owner_of(int64_t a, int64_t total, int G) {
+    return (int)(((a + 1) * G - 1) / total);
+}
+
+// Whether CTA c's range is non-empty (always, unless the phase has fewer
+// (m-tile, k-block) pairs than CTAs).
+__device__ __forceinline__ bool has_work(int64_t total, int G, int c) {
+    return total * (c + 1) / G > total * c / G;
+}
+
+// The units (m-tile, k-block range) of CTA c in a phase, in k order.
+struct Units {
+    int64_t idx, hi;
+    int nkb;
+    __device__ __forceinline__ Units() : idx(0), hi(0), nkb(1) {}
+    __device__ __forceinline__ Units(const Phase& ph, int G, int c)
+        : idx(ph.total * c / G), hi(ph.total * (c + 1) / G), nkb(ph.nkb) {}
+    __device__ __forceinline__ bool next(int& mt, int& kb0, int& kb1) {
+        if (idx >= hi) return false;
+        mt = (int)(idx / nkb);
+        kb0 = (int)(idx - (int64_t)mt * nkb);
+        kb1 = (int)min((int64_t)nkb, (int64_t)kb0 + (hi - idx));
+        idx += kb1 - kb0;
+        return true;
+    }
+};
+
+// Walks the weight tiles this CTA loads, in load order, across phases and
+// layers (a gate/up k-block is two tiles: gate, then up).
+struct TileCursor {
+    int k;
+    Phase ph;
+    Units u;
+    int mt, kb, kb1, hf;
+    const __nv_bfloat16* base;   // raw weight base of the tile last returned
+    __device__ __forceinline__ bool next(const FusedMaps& mp, const FusedParams& p, int G, int cta, int n_phases,
+                                         const CUtensorMap*& map, int& x, int& y) {
+        for (;;) {
+            if (kb < kb1) {
+                map = hf ? ph.wb : ph.wa;
+                base = hf ? ph.pb : ph.pa;
+                x = kb * 64;
+                y = mt * 128;
+                if (++hf == (ph.kind == K_GATEUP ? 2 : 1)) { hf = 0; ++kb; }
+                return true;
+            }
+            int kb0;
+            if (k >= 1 && u.next(mt, kb0, kb1)) { kb = kb0; hf = 0; continue; }
+            if (++k >= n_phases) return false;
+            ph = phase_of(mp, p, k);
+            u = Units(ph, G, cta);
+            kb = kb1 = 0;
+        }
+    }
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ float warp_sum32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Bounded wait until the grid barrier counter reaches target (acquire).
+__device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, volatile int* labort,
+                                       volatile int* gabort) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+        if (v >= target) return true;
+        if ((i & 15u) == 15u) {
+            if (*labort || *gabort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kFThreads, 1)
+fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
+    using C = FCfg<NP>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ctrl = smem + C::STAGES * C::STAGE;
+    uint64_t* full_w = reinterpret_cast<uint64_t*>(ctrl);
+    uint64_t* full_x = full_w + C::STAGES;
+    uint64_t* empty = full_x + C::STAGES;
+    uint64_t* acc_full = empty + C::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
+    volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(ctrl + 1008);
+    volatile unsigned* consumed = reinterpret_cast<volatile unsigned*>(ctrl + 1012);   // weight tiles the MMA has used
+    float* scale = reinterpret_cast<float*>(ctrl + C::CTRL);    // [128] RMSNorm scales of the phase input
+    int* seg = reinterpret_cast<int*>(scale + 128);             // partial slots of the tile being finalized
+    volatile int* seg_info = seg + kFusedGridCap;               // [nseg, jseg]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G, cta = blockIdx.x;
+    const int n_phases = 1 + 4 * p.L;
+    volatile int* gabort = p.gabort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_addr(&full_w[s]), 1);
+            mbar_init(smem_addr(&full_x[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&acc_full[a]), 1);
+            mbar_init(smem_addr(&acc_empty[a]), 4);
+        }
+        mbar_init(smem_addr(drain), 1);
+        *labort = 0;
+        *last_flag = 0;
+        *consumed = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *labort = 1;
+        atomicExch(p.gabort, 1);
+        if (p.err) atomicOr(p.err, TPL_DEVERR_TIMEOUT);
+    };
+
+    if (warp == kWarpW) {
+        // ---------------------------------------------------- weight producer
+        // Loads every weight tile of this CTA into the ring, across phase and
+        // layer boundaries (weights never depend on activations).
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            TileCursor ld{};
+            int stage = 0;
+            uint32_t par = 0;
+            int last_par[C::STAGES];           // parity of the latest copy issued into each stage, -1: none
+            for (int s = 0; s < C::STAGES; ++s) last_par[s] = -1;
+            const CUtensorMap* map;
+            int x, y;
+            bool ok = true;
+            while (ok && ld.next(mp, p, G, cta, n_phases, map, x, y)) {
+                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort)) { ok = false; break; }
+                const uint32_t fb = smem_addr(&full_w[stage]);
+                mbar_expect_tx(fb, C::W_BYTES);
+                tma_load_hint(smem_addr(smem + stage * C::STAGE), map, fb, x, y, pol);
+                last_par[stage] = (int)par;
+                if (++stage == C::STAGES) { stage = 0; par ^= 1; }
+            }
+            if (!ok) {
+                fail();
+                // let the copies already issued land before the CTA exits
+                for (int s = 0; s < C::STAGES; ++s) {
+                    if (last_par[s] < 0) continue;
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_addr(&full_w[s]), (uint32_t)last_par[s]) &&
+                           globaltimer() - t0 < kWaitLimitNs) {}
+                }
+            }
+        }
+    } else if (warp == kWarpAct) {
+        // ---------------------------------------------------- activation producer
+        // Fills the activation half of each stage once the phase's grid
+        // barrier has passed.  The second stage of a gate/up k-block reuses
+        // the first one's activations: its activation barrier still completes
+        // a phase (a plain arrive), so every barrier of the ring advances once
+        // per round and the parities stay in step.
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int stage = 0;
+            uint32_t par = 0;
+            int last_par[C::STAGES];
+            for (int s = 0; s < C::STAGES; ++s) last_par[s] = -1;
+            bool ok = true;
+            for (int k = 1; k < n_phases && ok; ++k) {
+                const Phase ph = phase_of(mp, p, k);
+                const int halves = ph.kind == K_GATEUP ? 2 : 1;
+                Units u(ph, G, cta);
+                int mt, kb0, kb1;
+                bool waited = false;
+                while (ok && u.next(mt, kb0, kb1)) {
+                    if (!waited) {
+                        if (!grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) { ok = false; break; }
+                        fence_proxy_async_global();
+                        waited = true;
+                    }
+                    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+                        for (int hf = 0; hf < halves; ++hf) {
+                            if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort)) { ok = false; break; }
+                            const uint32_t fb = smem_addr(&full_x[stage]);
+                            if (hf == 0) {
+                                mbar_expect_tx(fb, C::X_BYTES);
+                                tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, kb * 64, 0,
+                                              pol);
+                            } else {
+                                mbar_arrive(fb);
+                            }
+                            last_par[stage] = (int)par;
+                            if (++stage == C::STAGES) { stage = 0; par ^= 1; }
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                fail();
+                for (int s = 0; s < C::STAGES; ++s) {
+                    if (last_par[s] < 0) continue;
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_addr(&full_x[s]), (uint32_t)last_par[s]) &&
+                           globaltimer() - t0 < kWaitLimitNs) {}
+                }
+            }
+        }
+    } else if (warp == kWarpPf) {
+        // ---------------------------------------------------- L2 prefetch
+        // Walks the same weight tiles as the weight producer and brings each
+        // into L2 (one 128-byte line per tile row), up to kL2Ahead tiles ahead
+        // of the MMA, so HBM keeps streaming while phases wait on their grid
+        // barriers.  Stopping early (on an abort) only costs speed.
+        TileCursor pc{};
+        const CUtensorMap* map;
+        int x, y;
+        unsigned issued = 0;
+        while (pc.next(mp, p, G, cta, n_phases, map, x, y)) {
+            if (issued >= *consumed + (unsigned)kL2Ahead) {
+                const uint64_t t0 = globaltimer();
+                bool go = true;
+                while (issued >= *consumed + (unsigned)kL2Ahead) {
+                    if (*labort || *gabort || globaltimer() - t0 > kWaitLimitNs) { go = false; break; }
+                    __nanosleep(200);
+                }
+                if (!go) break;
+            }
+            const __nv_bfloat16* b = pc.base + x;
+            const int64_t K = pc.ph.K;
+            for (int r = lane; r < 128; r += 32)
+                if (y + r < pc.ph.M) prefetch_l2_line(b + (int64_t)(y + r) * K);
+            ++issued;
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(128, NP);
+            int stage = 0;
+            uint32_t par = 0;
+            int uc = 0;
+            bool ok = true;
+            for (int k = 1; k < n_phases && ok; ++k) {
+                const Phase ph = phase_of(mp, p, k);
+                const bool dual = ph.kind == K_GATEUP;
+                Units u(ph, G, cta);
+                int mt, kb0, kb1;
+                while (ok && u.next(mt, kb0, kb1)) {
+                    const int a = uc & 1;
+                    if (!mbar_wait(smem_addr(&acc_empty[a]), ((uc >> 1) & 1) ^ 1, labort, gabort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem + a * kAccStride;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(smem_addr(&full_w[stage]), par, labort, gabort) ||
+                            !mbar_wait(smem_addr(&full_x[stage]), par, labort, gabort)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sw = smem_addr(smem + stage * C::STAGE);
+                        const uint32_t sx = sw + C::W_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(d, sw128_desc(sw + kk * 32), sw128_desc(sx + kk * 32), idesc,
+                                     (kb > kb0 || kk > 0) ? 1u : 0u);
+                        int s2 = stage + 1;
+                        uint32_t p2 = par;
+                        if (s2 == C::STAGES) { s2 = 0; p2 ^= 1; }
+                        if (dual) {
+                            if (!mbar_wait(smem_addr(&full_w[s2]), p2, labort, gabort)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t sw2 = smem_addr(smem + s2 * C::STAGE);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16(d + NP, sw128_desc(sw2 + kk * 32), sw128_desc(sx + kk * 32), idesc,
+                                         (kb > kb0 || kk > 0) ? 1u : 0u);
+                            mma_commit(smem_addr(&empty[stage]));
+                            mma_commit(smem_addr(&empty[s2]));
+                            *consumed = *consumed + 2u;
+                            stage = s2 + 1;
+                            par = p2;
+                            if (stage == C::STAGES) { stage = 0; par ^= 1; }
+                        } else {
+                            mma_commit(smem_addr(&empty[stage]));
+                            *consumed = *consumed + 1u;
+                            stage = s2;
+                            par = p2;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_addr(&acc_full[a]));
+                    ++uc;
+                }
+            }
+            if (!ok) fail();
+            // every MMA issued above must complete before TMEM is released
+            mma_commit(smem_addr(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_addr(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {}
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..5)
+        // (warps 0, 1, 6 and 7 have their own roles above)
+        // Control flow is identical in all four warps, so the named barriers
+        // (bar 1, 128 threads) always match; after an abort the waits return
+        // at once and the memory work is skipped.
+        const int q = warp & 3;
+        const int row = q * 32 + lane;                 // drain: row of the tile (TMEM lane)
+        const bool leader = warp == 2 && lane == 0;
+        const int B = p.B, D = p.D;
+        const int Dt = (D + 127) / 128;
+        bool dead = false;
+
+        // phase 0: tile sums of squares of the launch input (warp per token)
+        for (int mt = cta; mt < Dt; mt += G) {
+            for (int t = q; t < B; t += 4) {
+                float ss = 0.f;
+                const int f = mt * 128 + lane * 4;
+                if (f < D) {
+                    const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p.x_in + (int64_t)t * D + f));
+                    const float a0 = __uint_as_float(v.x << 16), a1 = __uint_as_float(v.x & 0xFFFF0000u);
+                    const float a2 = __uint_as_float(v.y << 16), a3 = __uint_as_float(v.y & 0xFFFF0000u);
+                    ss = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+                }
+                ss = warp_sum32(ss);
+                if (lane == 0) p.slots_y[mt * B + t] = ss;
+            }
+        }
+        epi_sync();
+        if (leader) {
+            __threadfence();
+            atomicAdd(p.bar, 1u);
+        }
+
+        int uc = 0;
+        for (int k = 1; k < n_phases; ++k) {
+            const Phase ph = phase_of(mp, p, k);
+            const bool dual = ph.kind == K_GATEUP;
+            const int planes = dual ? 2 : 1;
+            const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
+            const int l = ph.layer;
+            Units u(ph, G, cta);
+            int mt, kb0, kb1;
+            if (normed && u.idx < u.hi) {
+                // RMSNorm scales of the phase input, while the first unit's
+                // MMAs run: every tile sum was written before this phase's
+                // grid barrier; thread per token
+                if (leader && !dead && !grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) fail();
+                epi_sync();
+                const float* sl = ph.kind == K_QKV ? p.slots_y : p.slots_h;
+                for (int t = row; t < B; t += 128) {
+                    float s = 0.f;
+#pragma unroll 4
+                    for (int m2 = 0; m2 < Dt; ++m2) s += __ldcg(sl + m2 * B + t);
+                    scale[t] = 1.0f / sqrtf(s / (float)D + p.eps);
+                }
+            }
+            // pass 1: drain every unit into its partial slot and count it on
+            // its tile's ticket (no waiting here, so tiles never wait on one
+            // another through a CTA that holds pieces of two of them)
+            while (u.next(mt, kb0, kb1)) {
+                const int a = uc & 1;
+                dead = dead || *labort || *gabort;
+                const bool got = dead ? false : mbar_wait(smem_addr(&acc_full[a]), (uc >> 1) & 1, labort, gabort);
+                dead = !__all_sync(0xFFFFFFFFu, got);
+                if (dead && lane == 0) fail();
+                float* slot = p.part + (size_t)(cta + mt) * C::PART_FLOATS;    // [plane][token][row]
+                if (!dead) {
+                    tc_fence_after();
+                    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
+                    for (int pl = 0; pl < planes; ++pl) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < NP && c0 < B; c0 += C::CH) {
+                            float v[32];
+                            if (C::CH == 32) tmem_ld32(tb + pl * NP + c0, v); else tmem_ld16(tb + pl * NP + c0, v);
+#pragma unroll
+                            for (int j = 0; j < C::CH; ++j)
+                                if (c0 + j < B) slot[(pl * NP + c0 + j) * 128 + row] = v[j];
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&acc_empty[a]));
+                ++uc;
+                epi_sync();                     // this CTA's partial of the tile is written
+                if (leader && !dead) {
+                    __threadfence();
+                    atomicAdd(p.tickets + ph.kind * p.max_mt + mt, 1u);
+                }
+            }
+            // pass 2: once all of a tile's units have arrived (a tile ticket
+            // counts arrivals monotonically over the layers of the launch),
+            // the CTAs holding them (contiguous, skipping CTAs without work)
+            // each finalize a share of the tile's tokens
+            Units u2(ph, G, cta);
+            while (u2.next(mt, kb0, kb1)) {
+                // the tile's segments in k order: the CTAs from the owner of its
+                // first k-block to the owner of its last one, all of which hold
+                // work unless the phase has fewer pairs than CTAs (then warp 2
+                // lists the ones that do)
+                const bool every = ph.total >= G;
+                const int cf = owner_of((int64_t)mt * ph.nkb, ph.total, G);
+                const int cl = owner_of((int64_t)mt * ph.nkb + ph.nkb - 1, ph.total, G);
+                if (!every && warp == 2) {
+                    int n = 0, j = 0;
+                    for (int base = cf; base <= cl; base += 32) {
+                        const int cc = base + lane;
+                        const bool w = cc <= cl && has_work(ph.total, G, cc);
+                        const unsigned m = __ballot_sync(0xFFFFFFFFu, w);
+                        if (w) seg[n + __popc(m & ((1u << lane) - 1u))] = cc + mt;
+                        n += __popc(m);
+                        j += __popc(__ballot_sync(0xFFFFFFFFu, w && cc < cta));
+                    }
+                    if (lane == 0) { seg_info[0] = n; seg_info[1] = j; }
+                }
+                epi_sync();
+                const int nseg = every ? cl - cf + 1 : seg_info[0];
+                const int jseg = every ? cta - cf : seg_info[1];
+                auto slot_of = [&](int j) { return every ? cf + j + mt : seg[j]; };
+                if (leader && !dead &&
+                    !grid_wait(p.tickets + ph.kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort))
+                    fail();
+                epi_sync();                     // every segment of the tile is visible
+                if (dead || *labort) { epi_sync(); continue; }
+
+                // this CTA's share of the tile's tokens; warp per token, lane
+                // per 4 consecutive rows; segments added in k order, all loads
+                // of a token issued before the sum
+                const int t_lo = (int)((int64_t)B * jseg / nseg), t_hi = (int)((int64_t)B * (jseg + 1) / nseg);
+                const int r0 = mt * 128 + lane * 4;
+                const __nv_bfloat16* resid = ph.kind == K_OPROJ
+                    ? (l == 0 ? p.x_in : (((l - 1) & 1) ? p.R1 : p.R0)) : p.h;
+                __nv_bfloat16* dst = ph.kind == K_OPROJ ? p.h : (l == p.L - 1 ? p.y_out : ((l & 1) ? p.R1 : p.R0));
+                const float* pbase = p.part + lane * 4;
+                auto emit = [&](int t, const float4& acc, const float4& acc2) {
+                    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+                    if (ph.kind == K_QKV) {
+                        const float s = scale[t];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (r0 + e < p.n_qkv) store_qkv(p.qkv, t, r0 + e, av[e] * s, 1);
+                    } else if (ph.kind == K_GATEUP) {
+                        if (r0 < p.F) {
+                            const float s = scale[t];
+                            const float uv[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
+                            __nv_bfloat16 hb[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) hb[e] = __float2bfloat16_rn(silu_f(av[e] * s) * (uv[e] * s));
+                            uint2 w;
+                            w.x = (uint32_t)__bfloat16_as_ushort(hb[0]) | ((uint32_t)__bfloat16_as_ushort(hb[1]) << 16);
+                            w.y = (uint32_t)__bfloat16_as_ushort(hb[2]) | ((uint32_t)__bfloat16_as_ushort(hb[3]) << 16);
+                            *reinterpret_cast<uint2*>(p.H + (int64_t)t * p.F + r0) = w;
+                        }
+                    } else {
+                        // residual add; the rounded values also feed the next RMSNorm
+                        float ss = 0.f;
+                        if (r0 < D) {
+                            const uint2 rv = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
+                            const float rr[4] = {__uint_as_float(rv.x << 16), __uint_as_float(rv.x & 0xFFFF0000u),
+                                                 __uint_as_float(rv.y << 16), __uint_as_float(rv.y & 0xFFFF0000u)};
+                            __nv_bfloat16 hb[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                hb[e] = __float2bfloat16_rn(rr[e] + av[e]);
+                                const float hv = __bfloat162float(hb[e]);
+                                ss = fmaf(hv, hv, ss);
+                            }
+                            uint2 w;
+                            w.x = (uint32_t)__bfloat16_as_ushort(hb[0]) | ((uint32_t)__bfloat16_as_ushort(hb[1]) << 16);
+                            w.y = (uint32_t)__bfloat16_as_ushort(hb[2]) | ((uint32_t)__bfloat16_as_ushort(hb[3]) << 16);
+                            *reinterpret_cast<uint2*>(dst + (int64_t)t * D + r0) = w;
+                        }
+                        ss = warp_sum32(ss);
+                        if (lane == 0) (ph.kind == K_OPROJ ? p.slots_h : p.slots_y)[mt * B + t] = ss;
+                    }
+                };
+                auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
+                constexpr int SC = 8;               // segment loads in flight per token
+                if (!dual) {
+                    // two tokens per warp per step
+                    for (int tA = t_lo + q; tA < t_hi; tA += 8) {
+                        const int tB = tA + 4;
+                        const bool hasB = tB < t_hi;
+                        float4 aA = make_float4(0.f, 0.f, 0.f, 0.f), aB = aA;
+                        for (int j0 = 0; j0 < nseg; j0 += SC) {
+                            float4 vA[SC], vB[SC];
+#pragma unroll
+                            for (int j = 0; j < SC; ++j) {
+                                if (j0 + j < nseg) {
+                                    const float* sp = pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS;
+                                    vA[j] = __ldcg(reinterpret_cast<const float4*>(sp + tA * 128));
+                                    if (hasB) vB[j] = __ldcg(reinterpret_cast<const float4*>(sp + tB * 128));
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < SC; ++j) {
+                                if (j0 + j < nseg) {
+                                    add4(aA, vA[j]);
+                                    if (hasB) add4(aB, vB[j]);
+                                }
+                            }
+                        }
+                        emit(tA, aA, aA);
+                        if (__any_sync(0xFFFFFFFFu, hasB) && hasB) emit(tB, aB, aB);
+                    }
+                } else {
+                    for (int t = t_lo + q; t < t_hi; t += 4) {
+                        float4 ag = make_float4(0.f, 0.f, 0.f, 0.f), au = ag;
+                        for (int j0 = 0; j0 < nseg; j0 += SC) {
+                            float4 vg[SC], vu[SC];
+#pragma unroll
+                            for (int j = 0; j < SC; ++j) {
+                                if (j0 + j < nseg) {
+                                    const float* sp = pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS;
+                                    vg[j] = __ldcg(reinterpret_cast<const float4*>(sp + t * 128));
+                                    vu[j] = __ldcg(reinterpret_cast<const float4*>(sp + (NP + t) * 128));
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < SC; ++j) {
+                                if (j0 + j < nseg) {
+                                    add4(ag, vg[j]);
+                                    add4(au, vu[j]);
+                                }
+                            }
+                        }
+                        emit(t, ag, au);
+                    }
+                }
+                fence_proxy_async_global();     // the next phase reads these outputs with TMA
+                epi_sync();                     // seg[] is rewritten for the next tile
+            }
+            // This CTA's part of phase k is done (including its token shares).
+            // The counter counts completions of all phases, so a CTA signals
+            // phase k only once barrier k has passed (a CTA with no work in a
+            // phase gets here without having waited for it): then
+            // bar >= G (k+1) means that every CTA has finished phases 0..k.
+            epi_sync();
+            if (leader && !dead) {
+                if (grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) {
+                    __threadfence();
+                    atomicAdd(p.bar, 1u);
+                } else {
+                    fail();
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int np_for(int64_t B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : 128; }
+
+template <int NP>
+int fused_smem() { return FCfg<NP>::SMEM; }
+
+int smem_for(int np) {
+    switch (np) {
+    case 16: return fused_smem<16>();
+    case 32: return fused_smem<32>();
+    case 64: return fused_smem<64>();
+    default: return fused_smem<128>();
+    }
+}
+
+struct FusedPlan {
+    int np, max_mt;
+    size_t ctrl_off, tick_off, sy_off, sh_off, r0_off, r1_off, o_off, h_off, hid_off, qkv_off, part_off, total;
+};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+FusedPlan plan_fused(const FusedShape& s) {
+    FusedPlan f{};
+    f.np = np_for(s.B);
+    const int64_t n_qkv = (int64_t)(s.n_q + 2 * s.n_kv) * s.hd;
+    const int64_t ko = (int64_t)s.n_q * s.hd;
+    const int64_t mts[4] = {(n_qkv + 127) / 128, (s.D + 127) / 128, (s.F + 127) / 128, (s.D + 127) / 128};
+    f.max_mt = (int)*std::max_element(mts, mts + 4);
+    const int64_t Dt = (s.D + 127) / 128;
+    const int kv_s = s.tp <= s.n_kv ? s.n_kv / s.tp : 1;
+    const int64_t w_s = (int64_t)(s.n_q / s.tp + 2 * kv_s) * s.hd;
+    size_t o = 0;
+    f.ctrl_off = o; o += 256;
+    f.tick_off = o; o += up256((size_t)4 * f.max_mt * 4);
+    f.sy_off = o; o += up256((size_t)Dt * s.B * 4);
+    f.sh_off = o; o += up256((size_t)Dt * s.B * 4);
+    f.r0_off = o; o += up256((size_t)s.B * s.D * 2);
+    f.r1_off = o; o += up256((size_t)s.B * s.D * 2);
+    f.o_off = o; o += up256((size_t)s.B * ko * 2);
+    f.h_off = o; o += up256((size_t)s.B * s.D * 2);
+    f.hid_off = o; o += up256((size_t)s.B * s.F * 2);
+    f.qkv_off = o; o += up256((size_t)s.tp * s.B * w_s * 2);
+    f.part_off = o; o += up256((size_t)(kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
+    f.total = o;
+    return f;
+}
+
+template <int NP>
+cudaError_t launch_np(const FusedMaps& maps, const FusedParams& prm, cudaStream_t st) {
+    using C = FCfg<NP>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)prm.G);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_stack_kernel<NP>, maps, prm);
+}
+
+}  // namespace
+
+bool fused_stack_shape_ok(const FusedShape& s) {
+    if (s.B < 1 || s.B > 128) return false;
+    if (s.D % 64 || s.F % 64 || ((int64_t)s.n_q * s.hd) % 64) return false;
+    return s.D <= (1 << 20) && s.F <= (1 << 20) && (int64_t)(s.n_q + 2 * s.n_kv) * s.hd <= (1 << 20);
+}
+
+size_t fused_stack_ws_bytes(const FusedShape& s) { return plan_fused(s).total; }
+
+cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, const void* const* Wqkv,
+                               const void* const* Wo, const void* const* Wg, const void* const* Wu,
+                               const void* const* Wd, int n_layers, void* ws, cudaStream_t st) {
+    const FusedPlan f = plan_fused(s);
+    const DeviceCtx* ctx = device_ctx();
+    if (!ctx) return cudaErrorNoDevice;
+    char* w = static_cast<char*>(ws);
+    const int64_t n_qkv = (int64_t)(s.n_q + 2 * s.n_kv) * s.hd;
+    const int64_t ko = (int64_t)s.n_q * s.hd;
+
+    int G = std::min(ctx->num_sms, kFusedGridCap);
+    {
+        int per_sm = 0;
+        const int smem = smem_for(f.np);
+        cudaError_t e = cudaSuccess;
+        switch (f.np) {
+        case 16: e = cudaFuncSetAttribute(fused_stack_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<16>, kFThreads, smem); break;
+        case 32: e = cudaFuncSetAttribute(fused_stack_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<32>, kFThreads, smem); break;
+        case 64: e = cudaFuncSetAttribute(fused_stack_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<64>, kFThreads, smem); break;
+        default: e = cudaFuncSetAttribute(fused_stack_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<128>, kFThreads, smem); break;
+        }
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        G = std::min(G, per_sm * ctx->num_sms);
+    }
+
+    FusedParams prm{};
+    prm.B = (int)s.B; prm.D = (int)s.D; prm.F = (int)s.F; prm.G = G;
+    prm.n_qkv = (int)n_qkv; prm.ko = (int)ko; prm.max_mt = f.max_mt; prm.eps = kRmsEpsilon;
+    const int kv_s = s.tp <= s.n_kv ? s.n_kv / s.tp : 1;
+    prm.qkv.n_q = s.n_q; prm.qkv.n_kv = s.n_kv; prm.qkv.head_dim = s.hd; prm.qkv.tp = s.tp;
+    prm.qkv.nq_s = s.n_q / s.tp; prm.qkv.kv_s = kv_s;
+    prm.qkv.w_s = (int64_t)(prm.qkv.nq_s + 2 * kv_s) * s.hd;
+    prm.qkv.shard_stride = s.B * prm.qkv.w_s;
+    prm.qkv.qkv_out = w + f.qkv_off;
+    prm.qkv.o_out = w + f.o_off;
+    prm.qkv.ldo_o = ko;
+    prm.R0 = reinterpret_cast<__nv_bfloat16*>(w + f.r0_off);
+    prm.R1 = reinterpret_cast<__nv_bfloat16*>(w + f.r1_off);
+    prm.O = reinterpret_cast<__nv_bfloat16*>(w + f.o_off);
+    prm.h = reinterpret_cast<__nv_bfloat16*>(w + f.h_off);
+    prm.H = reinterpret_cast<__nv_bfloat16*>(w + f.hid_off);
+    prm.slots_y = reinterpret_cast<float*>(w + f.sy_off);
+    prm.slots_h = reinterpret_cast<float*>(w + f.sh_off);
+    prm.part = reinterpret_cast<float*>(w + f.part_off);
+    prm.tickets = reinterpret_cast<unsigned*>(w + f.tick_off);
+    prm.bar = reinterpret_cast<unsigned*>(w + f.ctrl_off);
+    prm.gabort = reinterpret_cast<int*>(w + f.ctrl_off + 4);
+    prm.err = ctx->err_word;
+    prm.y_out = static_cast<__nv_bfloat16*>(y);
+
+    FusedMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int np = f.np;
+    if (!tma_map_bf16(&maps.act[A_R0], prm.R0, s.B, s.D, s.D, np) ||
+        !tma_map_bf16(&maps.act[A_R1], prm.R1, s.B, s.D, s.D, np) ||
+        !tma_map_bf16(&maps.act[A_O], prm.O, s.B, ko, ko, np) ||
+        !tma_map_bf16(&maps.act[A_H], prm.h, s.B, s.D, s.D, np) ||
+        !tma_map_bf16(&maps.act[A_HID], prm.H, s.B, s.F, s.F, np))
+        return cudaErrorInvalidValue;
+
+    for (int l0 = 0; l0 < n_layers; l0 += kFusedMaxLayers) {
+        const int L = std::min(kFusedMaxLayers, n_layers - l0);
+        const void* xin = l0 == 0 ? x : y;
+        prm.x_in = static_cast<const __nv_bfloat16*>(xin);
+        prm.L = L;
+        if (!tma_map_bf16(&maps.act[A_X], xin, s.B, s.D, s.D, np)) return cudaErrorInvalidValue;
+        for (int l = 0; l < L; ++l) {
+            prm.wptr[l][W_QKV] = static_cast<const __nv_bfloat16*>(Wqkv[l0 + l]);
+            prm.wptr[l][W_O] = static_cast<const __nv_bfloat16*>(Wo[l0 + l]);
+            prm.wptr[l][W_G] = static_cast<const __nv_bfloat16*>(Wg[l0 + l]);
+            prm.wptr[l][W_U] = static_cast<const __nv_bfloat16*>(Wu[l0 + l]);
+            prm.wptr[l][W_D] = static_cast<const __nv_bfloat16*>(Wd[l0 + l]);
+            if (!tma_map_bf16(&maps.w[l][W_QKV], Wqkv[l0 + l], n_qkv, s.D, s.D, 128) ||
+                !tma_map_bf16(&maps.w[l][W_O], Wo[l0 + l], s.D, ko, ko, 128) ||
+                !tma_map_bf16(&maps.w[l][W_G], Wg[l0 + l], s.F, s.D, s.D, 128) ||
+                !tma_map_bf16(&maps.w[l][W_U], Wu[l0 + l], s.F, s.D, s.D, 128) ||
+                !tma_map_bf16(&maps.w[l][W_D], Wd[l0 + l], s.D, s.F, s.F, 128))
+                return cudaErrorInvalidValue;
+        }
+        // grid barrier counter, abort flag and tickets start at zero
+        cudaError_t e = cudaMemsetAsync(w + f.ctrl_off, 0, f.sy_off - f.ctrl_off, st);
+        if (e != cudaSuccess) return e;
+        switch (np) {
+        case 16: e = launch_np<16>(maps, prm, st); break;
+        case 32: e = launch_np<32>(maps, prm, st); break;
+        case 64: e = launch_np<64>(maps, prm, st); break;
+        default: e = launch_np<128>(maps, prm, st); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace tpl

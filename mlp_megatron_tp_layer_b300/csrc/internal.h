@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -133,5 +134,26 @@ struct TcGemmArgs {
 };
 bool tc_gemm_supported();
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st);
+
+// TMA descriptor of a bf16 matrix [rows, cols] (row pitch ld elements), box
+// 64 columns x box_rows rows, 128-byte swizzle; cached per argument tuple.
+bool tma_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+
+// ------------------------------------------------ fused decode stack
+constexpr float kRmsEpsilon = 1e-6f;  // RMSNorm eps of the decoder composition
+constexpr int kFusedMaxLayers = 32;   // layers per launch (longer stacks take several launches)
+constexpr int kFusedGridCap = 148;    // CTAs per launch at most; the workspace is sized for it
+
+struct FusedShape {
+    int64_t B, D, F;
+    int n_q, n_kv, hd, tp;
+};
+// Shapes the fused decode stack handles (B <= 128, widths multiples of 64).
+bool fused_stack_shape_ok(const FusedShape& s);
+size_t fused_stack_ws_bytes(const FusedShape& s);
+// The whole stack in persistent cooperative launches (kFusedMaxLayers layers each).
+cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, const void* const* Wqkv,
+                               const void* const* Wo, const void* const* Wg, const void* const* Wu,
+                               const void* const* Wd, int n_layers, void* ws, cudaStream_t st);
 
 }  // namespace tpl

@@ -223,3 +223,37 @@ def test_decoder_stack_small(B):
     for W in layers:
         z = tpl.tp_decoder_layer(z, W, n_q, n_kv, hd, tp)
     assert_equal(y, to_np(z), what="stack vs layers")
+
+
+# ------------------------------------------------ fused decode stack
+
+@pytest.mark.parametrize("B", [1, 5, 16, 40, 100, 128])
+@pytest.mark.parametrize("path", [tpl.PATH_FUSED, tpl.PATH_UNFUSED])
+def test_decoder_stack_paths(B, path):
+    """Both implementations of the stack against the oracle; each deterministic."""
+    D, F, n_q, n_kv, hd, tp, L = 256, 512, 4, 2, 64, 2, 3
+    x = si.activations(B, D, seed=6, device="cuda")
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=6, layer=l, sigma=0.05, device="cuda") for l in range(L)]
+    trace = []
+    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                          trace=trace)
+    y1 = tpl.tp_decoder_stack(x, layers[:1], n_q, n_kv, hd, tp, path=path)
+    assert_within(y1, trace[1], stack_allowance(trace[:2], trace[1]), what="first layer")
+    y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, path=path)
+    assert_within(y, ref, stack_allowance(trace, ref), what="stack output")
+    y2 = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, path=path)
+    assert_equal(y2, to_np(y), what="second run")
+
+
+@pytest.mark.parametrize("B", [3, 64])
+def test_decoder_stack_fused_in_place_and_gqa_shapes(B):
+    """Fused stack with y == x, tp > n_kv (replicated KV groups) and hd 128."""
+    D, F, n_q, n_kv, hd, tp, L = 512, 1024, 8, 2, 128, 4, 2
+    x = si.activations(B, D, seed=8, device="cuda")
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=8, layer=l, sigma=0.04, device="cuda") for l in range(L)]
+    trace = []
+    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                          trace=trace)
+    y = x.clone()
+    tpl.tp_decoder_stack(y, layers, n_q, n_kv, hd, tp, out=y, path=tpl.PATH_FUSED)
+    assert_within(y, ref, stack_allowance(trace, ref), what="in-place fused stack")
