@@ -37,6 +37,7 @@ import synthetic_inputs as si  # noqa: E402
 
 METRIC = "decode weight-stream GB/s & prefill TFLOP/s per TP-sharded layer, 1×B300"
 QW = si.QWEN_DECODE
+LD = si.LLAMA_DECODE
 LP = si.LLAMA_PREFILL
 
 
@@ -45,6 +46,7 @@ def layer_bytes(D, F, n_q, n_kv, hd):
 
 
 QWEN_LAYER_BYTES = layer_bytes(QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"])
+LLAMA_LAYER_BYTES = layer_bytes(LD["D"], LD["F"], LD["n_q"], LD["n_kv"], LD["head_dim"])
 PREFILL_FLOPS = 2 * LP["B"] * LP["D"] * 2 * LP["F"] + 2 * LP["B"] * LP["F"] * LP["D"]
 
 
@@ -58,7 +60,8 @@ def args_parse():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
-    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--no-llama", action="store_true", help="skip the Llama-3.1-70B-shaped decode stack")
+    ap.add_argument("--only", choices=["decode", "prefill", "llama"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
     ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
@@ -390,6 +393,47 @@ def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     return out
 
 
+def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
+    """Llama-3.1-70B-shaped decode stack (8 layers, TP=8, 13.69 GB of weights),
+    one graph-replayed forward per batch size: weight-stream GB/s per batch."""
+    D, F, n_q, n_kv, hd, tp, L = LD["D"], LD["F"], LD["n_q"], LD["n_kv"], LD["head_dim"], LD["tp"], LD["n_layers"]
+    batches = list(LD["batches"])
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=0, layer=l, prefix="llama", device=dev) for l in range(L)]
+    xs = {B: si.activations(B, D, seed=3, name=f"llama.x{B}", device=dev) for B in batches}
+    ys = {B: torch.empty_like(xs[B]) for B in batches}
+    ws = tpl.workspace(max(tpl.decoder_workspace_bytes(B, D, F, n_q, n_kv, hd, tp) for B in batches), dev)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for B in batches:
+            tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws)
+    torch.cuda.synchronize()
+    for B in batches:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws)
+        graphs[B] = g
+    out = {"workload": f"Llama-3.1-70B-shaped decode stack: {L} layers D=8192 F=28672 64Q/8KV x128, TP=8 "
+                       f"logical shards, {L * LLAMA_LAYER_BYTES / 1e9:.2f} GB of weights per forward",
+           "per_batch": {}}
+    reps = max(3, args.steps // 4)
+    for B in batches:
+        for _ in range(2):
+            graphs[B].replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graphs[B].replay()
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / reps
+        gbs = L * LLAMA_LAYER_BYTES / (t / 1e3) / 1e9
+        out["per_batch"][str(B)] = {"ms_per_forward": t, "GB/s": gbs, "frac_of_peak": gbs / peaks["hbm_gbs"]}
+    del layers, graphs
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill(args, tpl, dev, world, peaks, peak_kind, stream):
     """Llama-3.1-70B-shaped prefill MLP (TP=8), fused shard reduce."""
     T = args.prefill_tokens
@@ -446,8 +490,16 @@ def main():
             print(json.dumps(dict(pre, metric=METRIC, n_gpus=world, steps=args.steps, warmup=args.warmup)),
                   flush=True)
         return
+    if args.only == "llama":
+        ll = run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream)
+        if rank == 0:
+            print(json.dumps(dict(ll, metric=METRIC, n_gpus=world, steps=args.steps)), flush=True)
+        return
 
     dec = run_decode(args, tpl, dev, world, peaks, peak_kind, stream)
+    llama = None
+    if not args.no_llama and args.only is None:
+        llama = run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream)
     prefill = None
     if not args.no_prefill and args.only is None:
         prefill = run_prefill(args, tpl, dev, world, peaks, peak_kind, stream)
@@ -469,7 +521,8 @@ def main():
                            "graphs": "one CUDA graph per batch size"},
                 "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
-                "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"], "prefill": prefill}
+                "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"], "llama_decode": llama,
+                "prefill": prefill}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -28,18 +28,17 @@
 // 0..k are complete everywhere.  The launch is cooperative, so every CTA is
 // resident and these waits (all bounded in time) can be met.  Weight tiles do
 // not depend on the activations, so the weight producer keeps loading the
-// next phase's weights into the shared-memory ring, and prefetching further
-// ones into L2, while the barrier is pending; only the activation loads wait
-// for it.
+// next phase's weights into the shared-memory ring while the barrier is
+// pending; only the activation loads wait for it.
 //
 // RMSNorm: the producer of a residual-stream value also writes, per 128-column
 // tile and token, the sum of squares of the rounded values; the consumer's
 // epilogue turns the tile sums into 1/rms and multiplies its fp32 products by
 // it (RMSNorm(x) W^T = diag(1/rms(x)) x W^T).
 //
-// Warp roles (256 threads): 0 weight TMA producer, 1 TMEM owner + MMA issuer,
+// Warp roles (224 threads): 0 weight TMA producer, 1 TMEM owner + MMA issuer,
 // 2..5 epilogue (warp w reads TMEM lanes 32 (w % 4) ..), 6 activation TMA
-// producer, 7 L2 prefetch of the weights ahead of the MMA.  Every wait is bounded in time; on expiry the CTA sets the grid
+// producer.  Every wait is bounded in time; on expiry the CTA sets the grid
 // abort flag and the sticky device error word, and every role winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,11 +53,10 @@
 namespace tpl {
 namespace {
 
-constexpr int kFThreads = 256;
-constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6, kWarpPf = 7;
+constexpr int kFThreads = 224;
+constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
-constexpr int kL2Ahead = 32;       // weight tiles prefetched into L2 ahead of the MMA
 enum Kind { K_QKV = 0, K_OPROJ = 1, K_GATEUP = 2, K_DOWN = 3 };
 enum ActMap { A_X = 0, A_R0 = 1, A_R1 = 2, A_O = 3, A_H = 4, A_HID = 5, A_COUNT = 6 };
 enum WMap { W_QKV = 0, W_O = 1, W_G = 2, W_U = 3, W_D = 4, W_COUNT = 5 };
@@ -84,7 +82,6 @@ struct FusedParams {
     unsigned* bar;             // grid barrier counter (zero at launch)
     int* gabort;               // grid abort flag (zero at launch)
     unsigned* err;
-    const __nv_bfloat16* wptr[kFusedMaxLayers][W_COUNT];   // weight bases (for L2 prefetch)
 };
 
 template <int NP>
@@ -105,10 +102,8 @@ struct FCfg {
 };
 
 struct Phase {
-    int kind, layer, m_tiles, nkb, M, K;
+    int kind, layer, m_tiles, nkb, M;
     int64_t total;
-    const __nv_bfloat16* pa;
-    const __nv_bfloat16* pb;
     const CUtensorMap* wa;
     const CUtensorMap* wb;
     const CUtensorMap* act;
@@ -138,9 +133,6 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     }
     ph.wa = &mp.w[l][wa];
     ph.wb = wb < 0 ? nullptr : &mp.w[l][wb];
-    ph.pa = p.wptr[l][wa];
-    ph.pb = wb < 0 ? nullptr : p.wptr[l][wb];
-    ph.K = K;
     ph.m_tiles = (ph.M + 127) / 128;
     ph.nkb = (K + 63) / 64;
     ph.total = (int64_t)ph.m_tiles * ph.nkb;
@@ -182,13 +174,11 @@ struct TileCursor {
     Phase ph;
     Units u;
     int mt, kb, kb1, hf;
-    const __nv_bfloat16* base;   // raw weight base of the tile last returned
     __device__ __forceinline__ bool next(const FusedMaps& mp, const FusedParams& p, int G, int cta, int n_phases,
                                          const CUtensorMap*& map, int& x, int& y) {
         for (;;) {
             if (kb < kb1) {
                 map = hf ? ph.wb : ph.wa;
-                base = hf ? ph.pb : ph.pa;
                 x = kb * 64;
                 y = mt * 128;
                 if (++hf == (ph.kind == K_GATEUP ? 2 : 1)) { hf = 0; ++kb; }
@@ -214,7 +204,13 @@ __device__ __forceinline__ float warp_sum32(float v) {
     return v;
 }
 
-// Bounded wait until the grid barrier counter reaches target (acquire).
+// Counter increment with release semantics: everything this thread (and,
+// through a preceding barrier, its CTA) wrote is visible before the count.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until a counter in global memory reaches target (acquire).
 __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, volatile int* labort,
                                        volatile int* gabort) {
     const uint64_t t0 = globaltimer();
@@ -226,7 +222,7 @@ __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, vol
             if (*labort || *gabort) return false;
             if (globaltimer() - t0 > kWaitLimitNs) return false;
         }
-        __nanosleep(64);
+        if (i > 64) __nanosleep(32);
     }
 }
 
@@ -246,7 +242,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
     volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
     volatile int* last_flag = reinterpret_cast<volatile int*>(ctrl + 1008);
-    volatile unsigned* consumed = reinterpret_cast<volatile unsigned*>(ctrl + 1012);   // weight tiles the MMA has used
     float* scale = reinterpret_cast<float*>(ctrl + C::CTRL);    // [128] RMSNorm scales of the phase input
     int* seg = reinterpret_cast<int*>(scale + 128);             // partial slots of the tile being finalized
     volatile int* seg_info = seg + kFusedGridCap;               // [nseg, jseg]
@@ -269,7 +264,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         mbar_init(smem_addr(drain), 1);
         *labort = 0;
         *last_flag = 0;
-        *consumed = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -371,32 +365,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 }
             }
         }
-    } else if (warp == kWarpPf) {
-        // ---------------------------------------------------- L2 prefetch
-        // Walks the same weight tiles as the weight producer and brings each
-        // into L2 (one 128-byte line per tile row), up to kL2Ahead tiles ahead
-        // of the MMA, so HBM keeps streaming while phases wait on their grid
-        // barriers.  Stopping early (on an abort) only costs speed.
-        TileCursor pc{};
-        const CUtensorMap* map;
-        int x, y;
-        unsigned issued = 0;
-        while (pc.next(mp, p, G, cta, n_phases, map, x, y)) {
-            if (issued >= *consumed + (unsigned)kL2Ahead) {
-                const uint64_t t0 = globaltimer();
-                bool go = true;
-                while (issued >= *consumed + (unsigned)kL2Ahead) {
-                    if (*labort || *gabort || globaltimer() - t0 > kWaitLimitNs) { go = false; break; }
-                    __nanosleep(200);
-                }
-                if (!go) break;
-            }
-            const __nv_bfloat16* b = pc.base + x;
-            const int64_t K = pc.ph.K;
-            for (int r = lane; r < 128; r += 32)
-                if (y + r < pc.ph.M) prefetch_l2_line(b + (int64_t)(y + r) * K);
-            ++issued;
-        }
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -438,13 +406,11 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                          (kb > kb0 || kk > 0) ? 1u : 0u);
                             mma_commit(smem_addr(&empty[stage]));
                             mma_commit(smem_addr(&empty[s2]));
-                            *consumed = *consumed + 2u;
                             stage = s2 + 1;
                             par = p2;
                             if (stage == C::STAGES) { stage = 0; par ^= 1; }
                         } else {
                             mma_commit(smem_addr(&empty[stage]));
-                            *consumed = *consumed + 1u;
                             stage = s2;
                             par = p2;
                         }
@@ -462,7 +428,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         }
     } else {
         // ---------------------------------------------------- epilogue (warps 2..5)
-        // (warps 0, 1, 6 and 7 have their own roles above)
+        // (warps 0, 1 and 6 have their own roles above)
         // Control flow is identical in all four warps, so the named barriers
         // (bar 1, 128 threads) always match; after an abort the waits return
         // at once and the memory work is skipped.
@@ -489,10 +455,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             }
         }
         epi_sync();
-        if (leader) {
-            __threadfence();
-            atomicAdd(p.bar, 1u);
-        }
+        if (leader) red_release_add(p.bar, 1u);
 
         int uc = 0;
         for (int k = 1; k < n_phases; ++k) {
@@ -546,10 +509,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (lane == 0) mbar_arrive(smem_addr(&acc_empty[a]));
                 ++uc;
                 epi_sync();                     // this CTA's partial of the tile is written
-                if (leader && !dead) {
-                    __threadfence();
-                    atomicAdd(p.tickets + ph.kind * p.max_mt + mt, 1u);
-                }
+                if (leader && !dead) red_release_add(p.tickets + ph.kind * p.max_mt + mt, 1u);
             }
             // pass 2: once all of a tile's units have arrived (a tile ticket
             // counts arrivals monotonically over the layers of the launch),
@@ -580,16 +540,18 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const int nseg = every ? cl - cf + 1 : seg_info[0];
                 const int jseg = every ? cta - cf : seg_info[1];
                 auto slot_of = [&](int j) { return every ? cf + j + mt : seg[j]; };
+                // this CTA's share of the tile's tokens (none for most CTAs
+                // when B is small: those do not wait for the tile)
+                const int t_lo = (int)((int64_t)B * jseg / nseg), t_hi = (int)((int64_t)B * (jseg + 1) / nseg);
+                if (t_lo == t_hi) { epi_sync(); continue; }
                 if (leader && !dead &&
                     !grid_wait(p.tickets + ph.kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort))
                     fail();
                 epi_sync();                     // every segment of the tile is visible
                 if (dead || *labort) { epi_sync(); continue; }
 
-                // this CTA's share of the tile's tokens; warp per token, lane
-                // per 4 consecutive rows; segments added in k order, all loads
-                // of a token issued before the sum
-                const int t_lo = (int)((int64_t)B * jseg / nseg), t_hi = (int)((int64_t)B * (jseg + 1) / nseg);
+                // warp per token, lane per 4 consecutive rows; segments added
+                // in k order, all loads of a token issued before the sum
                 const int r0 = mt * 128 + lane * 4;
                 const __nv_bfloat16* resid = ph.kind == K_OPROJ
                     ? (l == 0 ? p.x_in : (((l - 1) & 1) ? p.R1 : p.R0)) : p.h;
@@ -638,35 +600,25 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                 };
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
-                constexpr int SC = 8;               // segment loads in flight per token
                 if (!dual) {
-                    // two tokens per warp per step
-                    for (int tA = t_lo + q; tA < t_hi; tA += 8) {
-                        const int tB = tA + 4;
-                        const bool hasB = tB < t_hi;
-                        float4 aA = make_float4(0.f, 0.f, 0.f, 0.f), aB = aA;
+                    constexpr int SC = 16;          // segment loads in flight per token
+                    for (int t = t_lo + q; t < t_hi; t += 4) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int j0 = 0; j0 < nseg; j0 += SC) {
-                            float4 vA[SC], vB[SC];
+                            float4 v[SC];
 #pragma unroll
-                            for (int j = 0; j < SC; ++j) {
-                                if (j0 + j < nseg) {
-                                    const float* sp = pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS;
-                                    vA[j] = __ldcg(reinterpret_cast<const float4*>(sp + tA * 128));
-                                    if (hasB) vB[j] = __ldcg(reinterpret_cast<const float4*>(sp + tB * 128));
-                                }
-                            }
+                            for (int j = 0; j < SC; ++j)
+                                if (j0 + j < nseg)
+                                    v[j] = __ldcg(reinterpret_cast<const float4*>(
+                                        pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS + t * 128));
 #pragma unroll
-                            for (int j = 0; j < SC; ++j) {
-                                if (j0 + j < nseg) {
-                                    add4(aA, vA[j]);
-                                    if (hasB) add4(aB, vB[j]);
-                                }
-                            }
+                            for (int j = 0; j < SC; ++j)
+                                if (j0 + j < nseg) add4(acc, v[j]);
                         }
-                        emit(tA, aA, aA);
-                        if (__any_sync(0xFFFFFFFFu, hasB) && hasB) emit(tB, aB, aB);
+                        emit(t, acc, acc);
                     }
                 } else {
+                    constexpr int SC = 8;           // segment loads in flight per token and plane
                     for (int t = t_lo + q; t < t_hi; t += 4) {
                         float4 ag = make_float4(0.f, 0.f, 0.f, 0.f), au = ag;
                         for (int j0 = 0; j0 < nseg; j0 += SC) {
@@ -701,8 +653,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             epi_sync();
             if (leader && !dead) {
                 if (grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) {
-                    __threadfence();
-                    atomicAdd(p.bar, 1u);
+                    red_release_add(p.bar, 1u);
                 } else {
                     fail();
                 }
@@ -864,11 +815,6 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
         prm.L = L;
         if (!tma_map_bf16(&maps.act[A_X], xin, s.B, s.D, s.D, np)) return cudaErrorInvalidValue;
         for (int l = 0; l < L; ++l) {
-            prm.wptr[l][W_QKV] = static_cast<const __nv_bfloat16*>(Wqkv[l0 + l]);
-            prm.wptr[l][W_O] = static_cast<const __nv_bfloat16*>(Wo[l0 + l]);
-            prm.wptr[l][W_G] = static_cast<const __nv_bfloat16*>(Wg[l0 + l]);
-            prm.wptr[l][W_U] = static_cast<const __nv_bfloat16*>(Wu[l0 + l]);
-            prm.wptr[l][W_D] = static_cast<const __nv_bfloat16*>(Wd[l0 + l]);
             if (!tma_map_bf16(&maps.w[l][W_QKV], Wqkv[l0 + l], n_qkv, s.D, s.D, 128) ||
                 !tma_map_bf16(&maps.w[l][W_O], Wo[l0 + l], s.D, ko, ko, 128) ||
                 !tma_map_bf16(&maps.w[l][W_G], Wg[l0 + l], s.F, s.D, s.D, 128) ||
