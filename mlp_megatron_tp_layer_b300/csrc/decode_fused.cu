@@ -557,7 +557,8 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     ? (l == 0 ? p.x_in : (((l - 1) & 1) ? p.R1 : p.R0)) : p.h;
                 __nv_bfloat16* dst = ph.kind == K_OPROJ ? p.h : (l == p.L - 1 ? p.y_out : ((l & 1) ? p.R1 : p.R0));
                 const float* pbase = p.part + lane * 4;
-                auto emit = [&](int t, const float4& acc, const float4& acc2) {
+                const bool has_resid = ph.kind == K_OPROJ || ph.kind == K_DOWN;
+                auto emit = [&](int t, const float4& acc, const float4& acc2, const uint2& rv) {
                     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
                     if (ph.kind == K_QKV) {
                         const float s = scale[t];
@@ -580,7 +581,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                         // residual add; the rounded values also feed the next RMSNorm
                         float ss = 0.f;
                         if (r0 < D) {
-                            const uint2 rv = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
                             const float rr[4] = {__uint_as_float(rv.x << 16), __uint_as_float(rv.x & 0xFFFF0000u),
                                                  __uint_as_float(rv.y << 16), __uint_as_float(rv.y & 0xFFFF0000u)};
                             __nv_bfloat16 hb[4];
@@ -604,6 +604,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     constexpr int SC = 16;          // segment loads in flight per token
                     for (int t = t_lo + q; t < t_hi; t += 4) {
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        // the residual load travels with the partial loads
+                        const uint2 rv = (has_resid && r0 < D)
+                            ? __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0)) : make_uint2(0u, 0u);
                         for (int j0 = 0; j0 < nseg; j0 += SC) {
                             float4 v[SC];
 #pragma unroll
@@ -615,7 +618,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                             for (int j = 0; j < SC; ++j)
                                 if (j0 + j < nseg) add4(acc, v[j]);
                         }
-                        emit(t, acc, acc);
+                        emit(t, acc, acc, rv);
                     }
                 } else {
                     constexpr int SC = 8;           // segment loads in flight per token and plane
@@ -639,10 +642,12 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                 }
                             }
                         }
-                        emit(t, ag, au);
+                        emit(t, ag, au, make_uint2(0u, 0u));
                     }
                 }
-                fence_proxy_async_global();     // the next phase reads these outputs with TMA
+                // (the next phase reads these outputs with TMA: its activation
+                // producer acquires the grid barrier, which this CTA releases
+                // after these stores, and then fences the async proxy)
                 epi_sync();                     // seg[] is rewritten for the next tile
             }
             // This CTA's part of phase k is done (including its token shares).
