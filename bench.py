@@ -61,6 +61,7 @@ def args_parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-llama", action="store_true", help="skip the Llama-3.1-70B-shaped decode stack")
+    ap.add_argument("--no-cases", action="store_true", help="skip the sharded-matmul cases and shard_reduce")
     ap.add_argument("--only", choices=["decode", "prefill", "llama"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
@@ -434,6 +435,53 @@ def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     return out
 
 
+def time_ms(fn, reps):
+    """Average device time of fn over reps calls (CUDA events, after 3 warm-up calls)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_cases_and_reduce(args, tpl, dev, peaks, peak_kind):
+    """The four sharded-matmul cases at A[512,8192] . B[8192,28672], X = 8 (TFLOP/s,
+    bf16 output), and shard_reduce over 8 fp32 partial planes of a [4096, 8192] output."""
+    SC = si.SHARDED_CASES
+    d = si.sharded_case_operands(SC["I"], SC["J"], SC["K"], seed=0, device=dev)
+    flops = 2 * SC["I"] * SC["J"] * SC["K"]
+    cases = {}
+    for name, case, mode, gather in (("1", 1, 0, 0), ("2", 2, 0, 0), ("3 all-reduce", 3, 0, 0),
+                                     ("3 reduce-scatter", 3, 1, 0), ("3 via partials", 3, 0, 0),
+                                     ("4 gather B", 4, 0, 0), ("4 gather A", 4, 0, 1)):
+        want_p = name == "3 via partials"
+        P = torch.empty((SC["X"], SC["I"], SC["K"]), dtype=torch.float32, device=dev) if want_p else None
+        ws = tpl.workspace(tpl.case_workspace_bytes(case, mode, SC["I"], SC["J"], SC["K"], SC["X"]), dev)
+        k_sh = (case == 3 and mode == 1) or (case == 4 and gather == 1)
+        C = torch.empty((SC["X"], SC["I"], SC["K"] // SC["X"]) if k_sh else (SC["I"], SC["K"]), dtype=torch.bfloat16,
+                        device=dev)
+        t = time_ms(lambda: tpl.sharded_matmul(case, d["A"], d["Bt"], SC["X"], mode, gather, out=C,
+                                               partials=P if want_p else None, ws=ws), max(10, args.steps))
+        cases[name] = {"ms": t, "TFLOP/s": flops / (t / 1e3) / 1e12}
+    del d
+    rows, cols, tp = LP["B"], LP["D"], LP["tp"]
+    Pr = si.normal((tp, rows, cols), 1.0, 0, "bench.partials", torch.float32, device=dev)
+    Yr = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    t = time_ms(lambda: tpl.shard_reduce(Pr, tpl.ALLREDUCE, out=Yr), max(10, args.steps))
+    nbytes = tp * rows * cols * 4 + rows * cols * 2
+    red = {"workload": f"shard_reduce: {tp} fp32 planes [{rows}, {cols}] -> bf16", "ms": t,
+           "GB/s": nbytes / (t / 1e3) / 1e9, "frac_of_peak": nbytes / (t / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "peak_kind": peak_kind}
+    del Pr, Yr
+    return {"workload": f"sharded matmul A[{SC['I']},{SC['J']}] . B[{SC['J']},{SC['K']}], X={SC['X']}, bf16 out",
+            "per_case": cases}, red
+
+
 def run_prefill(args, tpl, dev, world, peaks, peak_kind, stream):
     """Llama-3.1-70B-shaped prefill MLP (TP=8), fused shard reduce."""
     T = args.prefill_tokens
@@ -504,6 +552,10 @@ def main():
     if not args.no_prefill and args.only is None:
         prefill = run_prefill(args, tpl, dev, world, peaks, peak_kind, stream)
 
+    cases = reduce_line = None
+    if not args.no_cases and args.only is None:
+        cases, reduce_line = run_cases_and_reduce(args, tpl, dev, peaks, peak_kind)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only is None:
         cpu = cpu_baseline(dec["layers"], args.cpu_seconds)
@@ -522,7 +574,7 @@ def main():
                 "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
                 "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"], "llama_decode": llama,
-                "prefill": prefill}
+                "prefill": prefill, "sharded_matmul": cases, "shard_reduce": reduce_line}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -45,6 +45,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -600,50 +601,63 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                 };
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
-                if (!dual) {
-                    constexpr int SC = 16;          // segment loads in flight per token
-                    for (int t = t_lo + q; t < t_hi; t += 4) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        // the residual load travels with the partial loads
-                        const uint2 rv = (has_resid && r0 < D)
-                            ? __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0)) : make_uint2(0u, 0u);
-                        for (int j0 = 0; j0 < nseg; j0 += SC) {
-                            float4 v[SC];
+                // A warp takes TB of its tokens at a time with up to SB segment
+                // loads in flight per token (per plane for gate/up), plus the
+                // residuals; segments are added in k order.  One token with 16
+                // loads suits few tokens and many segments (NP = 16); two
+                // tokens per round trip suit the larger batches.
+                auto share = [&](auto tb_c, auto sb_c, auto dual_c) {
+                    constexpr int TB = decltype(tb_c)::value, SB = decltype(sb_c)::value;
+                    constexpr bool DU = decltype(dual_c)::value;
+                    for (int t0 = t_lo + q; t0 < t_hi; t0 += 4 * TB) {
+                        float4 acc[TB], acc2[TB];
+                        uint2 rv[TB];
 #pragma unroll
-                            for (int j = 0; j < SC; ++j)
-                                if (j0 + j < nseg)
-                                    v[j] = __ldcg(reinterpret_cast<const float4*>(
-                                        pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS + t * 128));
-#pragma unroll
-                            for (int j = 0; j < SC; ++j)
-                                if (j0 + j < nseg) add4(acc, v[j]);
+                        for (int j = 0; j < TB; ++j) {
+                            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            acc2[j] = acc[j];
+                            rv[j] = make_uint2(0u, 0u);
+                            const int t = t0 + 4 * j;
+                            if (has_resid && t < t_hi && r0 < D)
+                                rv[j] = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
                         }
-                        emit(t, acc, acc, rv);
+                        for (int s0 = 0; s0 < nseg; s0 += SB) {
+                            float4 v[TB][SB], w[DU ? TB : 1][DU ? SB : 1];
+#pragma unroll
+                            for (int j = 0; j < TB; ++j)
+#pragma unroll
+                                for (int k2 = 0; k2 < SB; ++k2) {
+                                    const int t = t0 + 4 * j;
+                                    if (t < t_hi && s0 + k2 < nseg) {
+                                        const float* sp = pbase + (size_t)slot_of(s0 + k2) * C::PART_FLOATS;
+                                        v[j][k2] = __ldcg(reinterpret_cast<const float4*>(sp + t * 128));
+                                        if constexpr (DU)
+                                            w[j][k2] = __ldcg(reinterpret_cast<const float4*>(sp + (NP + t) * 128));
+                                    }
+                                }
+#pragma unroll
+                            for (int j = 0; j < TB; ++j)
+#pragma unroll
+                                for (int k2 = 0; k2 < SB; ++k2)
+                                    if (t0 + 4 * j < t_hi && s0 + k2 < nseg) {
+                                        add4(acc[j], v[j][k2]);
+                                        if constexpr (DU) add4(acc2[j], w[j][k2]);
+                                    }
+                        }
+#pragma unroll
+                        for (int j = 0; j < TB; ++j)
+                            if (t0 + 4 * j < t_hi) emit(t0 + 4 * j, acc[j], acc2[j], rv[j]);
                     }
+                };
+                using I1 = std::integral_constant<int, 1>;
+                using I2 = std::integral_constant<int, 2>;
+                using I4 = std::integral_constant<int, 4>;
+                using I8 = std::integral_constant<int, 8>;
+                using I16 = std::integral_constant<int, 16>;
+                if constexpr (NP == 16) {
+                    if (!dual) share(I1{}, I16{}, std::false_type{}); else share(I1{}, I8{}, std::true_type{});
                 } else {
-                    constexpr int SC = 8;           // segment loads in flight per token and plane
-                    for (int t = t_lo + q; t < t_hi; t += 4) {
-                        float4 ag = make_float4(0.f, 0.f, 0.f, 0.f), au = ag;
-                        for (int j0 = 0; j0 < nseg; j0 += SC) {
-                            float4 vg[SC], vu[SC];
-#pragma unroll
-                            for (int j = 0; j < SC; ++j) {
-                                if (j0 + j < nseg) {
-                                    const float* sp = pbase + (size_t)slot_of(j0 + j) * C::PART_FLOATS;
-                                    vg[j] = __ldcg(reinterpret_cast<const float4*>(sp + t * 128));
-                                    vu[j] = __ldcg(reinterpret_cast<const float4*>(sp + (NP + t) * 128));
-                                }
-                            }
-#pragma unroll
-                            for (int j = 0; j < SC; ++j) {
-                                if (j0 + j < nseg) {
-                                    add4(ag, vg[j]);
-                                    add4(au, vu[j]);
-                                }
-                            }
-                        }
-                        emit(t, ag, au, make_uint2(0u, 0u));
-                    }
+                    if (!dual) share(I2{}, I8{}, std::false_type{}); else share(I2{}, I4{}, std::true_type{});
                 }
                 // (the next phase reads these outputs with TMA: its activation
                 // producer acquires the grid barrier, which this CTA releases
