@@ -156,6 +156,37 @@ class ClockSampler:
                 "samples": len(loaded), "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
 
 
+FUSED_SOURCES = ("decode_fused.cu", "ptx.cuh", "epilogue.cuh", "internal.h")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_stack_traffic.txt")
+
+
+def fused_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in FUSED_SOURCES:
+        with open(os.path.join(ROOT, "mlp_megatron_tp_layer_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def fused_traffic(batches):
+    """Mean DRAM bytes per launch of the fused stack over the given batch sizes,
+    from the committed ncu summary, or None if it is missing or was taken on
+    different kernel sources."""
+    try:
+        kv = dict(line.strip().split("=", 1) for line in open(TRAFFIC_FILE)
+                  if "=" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    if kv.get("source_sha256_16") != fused_source_hash():
+        return None
+    try:
+        vals = [float(kv[f"qwen_28_layers_b{B}"]) for B in batches]
+    except KeyError:
+        return None
+    return sum(vals) / len(vals)
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -372,8 +403,9 @@ def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
         total_bytes = sum(alg[dom](B) for B in batches)
         n_launch, t_ms = tot[dom]
         achieved = total_bytes / (t_ms / 1e3) / 1e9
+        traffic = fused_traffic(batches) if dom == "fused_stack" and L == QW["n_layers"] else None
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
                 "launches": n_launch, "avg_launch_us": t_ms / n_launch * 1e3,
                 "algorithmic_bytes_per_launch_avg": total_bytes / n_launch}
     share = {k: {"launches": v[0], "ms": v[1], "share": v[1] / sum(x[1] for x in tot.values())}
