@@ -426,6 +426,30 @@ def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     return out
 
 
+def run_parallel_block(args, tpl, dev, layers, peaks, stream):
+    """The same Qwen-shaped stack in the parallel (PaLM) arrangement of the
+    pages (y = x + Attn(RMSNorm x) + MLP(RMSNorm x), one shared reduction per
+    layer): weight-stream GB/s per batch size, graph-replayed."""
+    D, F, n_q, n_kv, hd, tp = QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"]
+    L = len(layers)
+    out = {"workload": f"Qwen2.5-1.5B-shaped decode, parallel block, {L} layers, TP=2", "per_batch": {}}
+    for B in QW["batches"]:
+        x = si.activations(B, D, seed=1, name=f"bench.x{B}", device=dev)
+        y = torch.empty_like(x)
+        ws = tpl.workspace(tpl.decoder_workspace_bytes(B, D, F, n_q, n_kv, hd, tp), dev)
+        with torch.cuda.stream(stream):
+            tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, out=y, ws=ws, block=tpl.BLOCK_PARALLEL)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, out=y, ws=ws, block=tpl.BLOCK_PARALLEL)
+        t = time_ms(g.replay, max(5, args.steps // 2))
+        gbs = L * QWEN_LAYER_BYTES / (t / 1e3) / 1e9
+        out["per_batch"][str(B)] = {"ms_per_forward": t, "GB/s": gbs, "frac_of_peak": gbs / peaks["hbm_gbs"]}
+        del g
+    return out
+
+
 def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     """Llama-3.1-70B-shaped decode stack (8 layers, TP=8, 13.69 GB of weights),
     one graph-replayed forward per batch size: weight-stream GB/s per batch."""
@@ -577,6 +601,9 @@ def main():
         return
 
     dec = run_decode(args, tpl, dev, world, peaks, peak_kind, stream)
+    parallel = None
+    if args.only is None:
+        parallel = run_parallel_block(args, tpl, dev, dec["layers"], peaks, stream)
     llama = None
     if not args.no_llama and args.only is None:
         llama = run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream)
@@ -605,7 +632,8 @@ def main():
                            "graphs": "one CUDA graph per batch size"},
                 "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
-                "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"], "llama_decode": llama,
+                "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"],
+                "qwen_decode_parallel_block": parallel, "llama_decode": llama,
                 "prefill": prefill, "sharded_matmul": cases, "shard_reduce": reduce_line}
         print(json.dumps(line), flush=True)
     if world > 1:

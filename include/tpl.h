@@ -254,6 +254,14 @@ tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv,
                                 const void* const* Wu, const void* const* Wd, int n_layers,
                                 int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int head_dim,
                                 int tp, void* ws, size_t ws_bytes, void* stream);
+/* Block arrangement ([L4] S5.5).  SERIAL: the pre-norm block above.  PARALLEL
+ * (PaLM): y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)); both sublayers read the
+ * same normalised input and their shard partials are summed together with x in
+ * one reduction (the pages' shared all-reduce), so the fused stack needs two
+ * grid-wide exchanges per layer instead of four.  PARALLEL runs on the FUSED
+ * implementation only (TPL_ERR_UNSUPPORTED where it does not apply). */
+typedef enum tpl_block { TPL_BLOCK_SERIAL = 0, TPL_BLOCK_PARALLEL = 1 } tpl_block;
+
 /* tp_decoder_stack with the implementation chosen by `path` (tpl_decode_path). */
 tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
                                      const void* const* Wo, const void* const* Wg,
@@ -261,6 +269,14 @@ tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* 
                                      int64_t B, int64_t D, int64_t F, int n_q, int n_kv,
                                      int head_dim, int tp, void* ws, size_t ws_bytes, int path,
                                      void* stream);
+/* tp_decoder_stack with both the implementation (`path`) and the block
+ * arrangement (`block`, tpl_block) chosen. */
+tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void* const* Wqkv,
+                                   const void* const* Wo, const void* const* Wg,
+                                   const void* const* Wu, const void* const* Wd, int n_layers,
+                                   int64_t B, int64_t D, int64_t F, int n_q, int n_kv, int head_dim,
+                                   int tp, void* ws, size_t ws_bytes, int path, int block,
+                                   void* stream);
 
 /* --------------------------------------------------------------------------
  * Launch timing, for measurement only (off by default).

@@ -24,6 +24,7 @@ F32, BF16 = 0, 1
 ALLREDUCE, REDUCE_SCATTER = 0, 1
 GATHER_B, GATHER_A = 0, 1
 PATH_AUTO, PATH_UNFUSED, PATH_FUSED = 0, 1, 2
+BLOCK_SERIAL, BLOCK_PARALLEL = 0, 1
 STATUS = {0: "TPL_OK", 1: "TPL_ERR_NULL", 2: "TPL_ERR_SHAPE", 3: "TPL_ERR_ALIGN", 4: "TPL_ERR_DTYPE",
           5: "TPL_ERR_WORKSPACE", 6: "TPL_ERR_UNSUPPORTED", 7: "TPL_ERR_CUDA", 8: "TPL_ERR_TIMEOUT",
           9: "TPL_ERR_ALIAS", 10: "TPL_ERR_STATIC_LIMIT"}
@@ -53,6 +54,9 @@ _SIGS = {
     "tpl_tp_decoder_stack_path": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
                                          _i32, _i32, _i32, _vp, _sz, _i32, _vp]),
+    "tpl_tp_decoder_stack_ex": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                       ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
+                                       _i32, _i32, _i32, _vp, _sz, _i32, _i32, _vp]),
     "tpl_tp_decoder_layer": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32,
                                     _i32, _vp, _sz, _vp]),
     "tpl_tp_decoder_stack": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
@@ -314,9 +318,11 @@ def _ptr_array(ts):
     return arr
 
 
-def tp_decoder_stack(x, layers, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=None, path=PATH_AUTO):
-    """Serial pre-norm decoder layers; ``layers`` is a list of dicts with Wqkv, Wo, Wg, Wu, Wd.
-    ``path``: PATH_AUTO (fused where it applies), PATH_UNFUSED or PATH_FUSED."""
+def tp_decoder_stack(x, layers, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=None, path=PATH_AUTO,
+                     block=BLOCK_SERIAL):
+    """Decoder layers; ``layers`` is a list of dicts with Wqkv, Wo, Wg, Wu, Wd.
+    ``path``: PATH_AUTO (fused where it applies), PATH_UNFUSED or PATH_FUSED.
+    ``block``: BLOCK_SERIAL (pre-norm) or BLOCK_PARALLEL (x + Attn(RMSNorm x) + MLP(RMSNorm x))."""
     _contig(x)
     B, D = x.shape
     F = layers[0]["Wg"].shape[0]
@@ -325,9 +331,9 @@ def tp_decoder_stack(x, layers, n_q, n_kv, head_dim, tp, out=None, ws=None, stre
     nbytes = decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp)
     ws = workspace(nbytes, x.device) if ws is None else ws
     arrs = [_ptr_array([L[k] for L in layers]) for k in ("Wqkv", "Wo", "Wg", "Wu", "Wd")]
-    _check(lib.tpl_tp_decoder_stack_path(_p(x), _p(out), *arrs, len(layers), B, D, F, n_q, n_kv, head_dim, tp,
-                                         _p(ws), ws.numel() * ws.element_size(), path, _stream(stream)),
-           "tpl_tp_decoder_stack_path")
+    _check(lib.tpl_tp_decoder_stack_ex(_p(x), _p(out), *arrs, len(layers), B, D, F, n_q, n_kv, head_dim, tp,
+                                       _p(ws), ws.numel() * ws.element_size(), path, block, _stream(stream)),
+           "tpl_tp_decoder_stack_ex")
     return out
 
 

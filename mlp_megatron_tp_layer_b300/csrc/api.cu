@@ -685,13 +685,15 @@ static tpl_status check_layer_args(const void* x, const void* y, const void* Wqk
     return TPL_OK;
 }
 
-extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
-                                                const void* const* Wo, const void* const* Wg, const void* const* Wu,
-                                                const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,
-                                                int n_q, int n_kv, int head_dim, int tp, void* ws, size_t ws_bytes,
-                                                int path, void* stream) {
+extern "C" tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void* const* Wqkv,
+                                              const void* const* Wo, const void* const* Wg, const void* const* Wu,
+                                              const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,
+                                              int n_q, int n_kv, int head_dim, int tp, void* ws, size_t ws_bytes,
+                                              int path, int block, void* stream) {
     if (!Wqkv || !Wo || !Wg || !Wu || !Wd || !ws) return TPL_ERR_NULL;
     if (path != TPL_PATH_AUTO && path != TPL_PATH_UNFUSED && path != TPL_PATH_FUSED) return TPL_ERR_UNSUPPORTED;
+    if (block != TPL_BLOCK_SERIAL && block != TPL_BLOCK_PARALLEL) return TPL_ERR_UNSUPPORTED;
+    if (block == TPL_BLOCK_PARALLEL && path == TPL_PATH_UNFUSED) return TPL_ERR_UNSUPPORTED;
     if (n_layers <= 0) return TPL_ERR_SHAPE;
     size_t need = 0;
     tpl_status s = tpl_tp_decoder_workspace(B, D, F, n_q, n_kv, head_dim, tp, &need);
@@ -709,10 +711,11 @@ extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const vo
     cudaStream_t st = S(stream);
     const FusedShape fs{B, D, F, n_q, n_kv, head_dim, tp};
     const bool fused_ok = fused_stack_shape_ok(fs) && tc_gemm_supported();
-    if (path == TPL_PATH_FUSED && !fused_ok) return TPL_ERR_UNSUPPORTED;
+    if ((path == TPL_PATH_FUSED || block == TPL_BLOCK_PARALLEL) && !fused_ok) return TPL_ERR_UNSUPPORTED;
     if (path != TPL_PATH_UNFUSED && fused_ok) {
         ProfScope prof("fused_stack", st);
-        return cuda_status(launch_fused_stack(fs, x, y, Wqkv, Wo, Wg, Wu, Wd, n_layers, ws, st));
+        return cuda_status(launch_fused_stack(fs, x, y, Wqkv, Wo, Wg, Wu, Wd, n_layers, block == TPL_BLOCK_PARALLEL,
+                                              ws, st));
     }
     for (int l = 0; l < n_layers; ++l) {
         // every layer after the first finds the RMSNorm scales of its input
@@ -722,6 +725,15 @@ extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const vo
         if (e != cudaSuccess) return TPL_ERR_CUDA;
     }
     return TPL_OK;
+}
+
+extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
+                                                const void* const* Wo, const void* const* Wg, const void* const* Wu,
+                                                const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,
+                                                int n_q, int n_kv, int head_dim, int tp, void* ws, size_t ws_bytes,
+                                                int path, void* stream) {
+    return tpl_tp_decoder_stack_ex(x, y, Wqkv, Wo, Wg, Wu, Wd, n_layers, B, D, F, n_q, n_kv, head_dim, tp, ws,
+                                   ws_bytes, path, TPL_BLOCK_SERIAL, stream);
 }
 
 extern "C" tpl_status tpl_tp_decoder_stack(const void* x, void* y, const void* const* Wqkv, const void* const* Wo,

@@ -70,6 +70,7 @@ struct FusedMaps {
 
 struct FusedParams {
     int B, D, F, L, G;
+    int parallel;              // 1: parallel block ([L4] S5.5), 0: serial pre-norm block
     int n_qkv, ko;             // packed QKV rows, o_proj input width n_q hd
     int max_mt;                // ticket row length
     float eps;
@@ -93,7 +94,7 @@ struct FCfg {
     static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int CTRL = 1024;                            // mbarriers and flags
-    static constexpr int EPI = 128 * 4 + (kFusedGridCap + 4) * 4;   // RMSNorm scales, segment list
+    static constexpr int EPI = 128 * 4 + (2 * kFusedGridCap + 8) * 4;   // RMSNorm scales, two segment lists
     static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI;
     static constexpr int PART_FLOATS = 2 * NP * 128;             // one partial slot
     static constexpr int CH = NP >= 32 ? 32 : 16;                // TMEM columns per load
@@ -104,18 +105,36 @@ struct FCfg {
 
 struct Phase {
     int kind, layer, m_tiles, nkb, M;
+    int stage;                 // grid-barrier stage the phase's activations wait for
+    bool last_of_stage;        // the CTA signals the stage after this phase
+    int region;                // partial-slot region (two phases of one stage must not share one)
     int64_t total;
     const CUtensorMap* wa;
     const CUtensorMap* wb;
     const CUtensorMap* act;
 };
 
-// Phase k >= 1 of the launch: layer (k-1)/4, projection (k-1)%4.
+// Phase k >= 1 of the launch: layer (k-1)/4, projection (k-1)%4.  Serial
+// block: QKV, o_proj, gate/up, down, each its own stage.  Parallel block: QKV
+// and gate/up (both on RMSNorm(x)) form one stage, o_proj and down (their
+// partials summed together into y) the next.
 __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams& p, int k) {
     Phase ph;
     ph.layer = (k - 1) >> 2;
-    ph.kind = (k - 1) & 3;
+    const int pos = (k - 1) & 3;
     const int l = ph.layer;
+    if (p.parallel) {
+        constexpr int order[4] = {K_QKV, K_GATEUP, K_OPROJ, K_DOWN};
+        ph.kind = order[pos];
+        ph.stage = 1 + 2 * l + (pos >> 1);
+        ph.last_of_stage = (pos & 1) != 0;
+        ph.region = (ph.kind == K_QKV || ph.kind == K_OPROJ) ? 1 : 0;
+    } else {
+        ph.kind = pos;
+        ph.stage = k;
+        ph.last_of_stage = true;
+        ph.region = 0;
+    }
     int K, wa, wb = -1;
     switch (ph.kind) {
     case K_QKV:
@@ -126,7 +145,8 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
         ph.M = p.D; K = p.ko; wa = W_O; ph.act = &mp.act[A_O];
         break;
     case K_GATEUP:
-        ph.M = p.F; K = p.D; wa = W_G; wb = W_U; ph.act = &mp.act[A_H];
+        ph.M = p.F; K = p.D; wa = W_G; wb = W_U;
+        ph.act = p.parallel ? &mp.act[l == 0 ? A_X : (((l - 1) & 1) ? A_R1 : A_R0)] : &mp.act[A_H];
         break;
     default:
         ph.M = p.D; K = p.F; wa = W_D; ph.act = &mp.act[A_HID];
@@ -245,7 +265,8 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     volatile int* last_flag = reinterpret_cast<volatile int*>(ctrl + 1008);
     float* scale = reinterpret_cast<float*>(ctrl + C::CTRL);    // [128] RMSNorm scales of the phase input
     int* seg = reinterpret_cast<int*>(scale + 128);             // partial slots of the tile being finalized
-    volatile int* seg_info = seg + kFusedGridCap;               // [nseg, jseg]
+    int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
+    volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, jseg, nseg2, jseg2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, cta = blockIdx.x;
@@ -335,7 +356,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 bool waited = false;
                 while (ok && u.next(mt, kb0, kb1)) {
                     if (!waited) {
-                        if (!grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) { ok = false; break; }
+                        if (!grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) { ok = false; break; }
                         fence_proxy_async_global();
                         waited = true;
                     }
@@ -465,15 +486,21 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const int planes = dual ? 2 : 1;
             const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
             const int l = ph.layer;
+            // parallel block: o_proj and down partials of a tile are added
+            // together (one reduction for both sublayers), so they share the
+            // down tile's ticket and its finalize
+            const bool merged = p.parallel && ph.kind == K_DOWN;
+            const int tk_kind = (p.parallel && ph.kind == K_OPROJ) ? K_DOWN : ph.kind;
             Units u(ph, G, cta);
             int mt, kb0, kb1;
             if (normed && u.idx < u.hi) {
                 // RMSNorm scales of the phase input, while the first unit's
                 // MMAs run: every tile sum was written before this phase's
                 // grid barrier; thread per token
-                if (leader && !dead && !grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) fail();
+                if (leader && !dead && !grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) fail();
                 epi_sync();
-                const float* sl = ph.kind == K_QKV ? p.slots_y : p.slots_h;
+                // the serial block's MLP normalises h, everything else the layer input
+                const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
                 for (int t = row; t < B; t += 128) {
                     float s = 0.f;
 #pragma unroll 4
@@ -490,7 +517,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const bool got = dead ? false : mbar_wait(smem_addr(&acc_full[a]), (uc >> 1) & 1, labort, gabort);
                 dead = !__all_sync(0xFFFFFFFFu, got);
                 if (dead && lane == 0) fail();
-                float* slot = p.part + (size_t)(cta + mt) * C::PART_FLOATS;    // [plane][token][row]
+                float* slot = p.part + ((size_t)ph.region * (kFusedGridCap + p.max_mt) + cta + mt) * C::PART_FLOATS;
                 if (!dead) {
                     tc_fence_after();
                     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
@@ -510,43 +537,62 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (lane == 0) mbar_arrive(smem_addr(&acc_empty[a]));
                 ++uc;
                 epi_sync();                     // this CTA's partial of the tile is written
-                if (leader && !dead) red_release_add(p.tickets + ph.kind * p.max_mt + mt, 1u);
+                if (leader && !dead) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
             }
             // pass 2: once all of a tile's units have arrived (a tile ticket
             // counts arrivals monotonically over the layers of the launch),
             // the CTAs holding them (contiguous, skipping CTAs without work)
             // each finalize a share of the tile's tokens
-            Units u2(ph, G, cta);
-            while (u2.next(mt, kb0, kb1)) {
-                // the tile's segments in k order: the CTAs from the owner of its
-                // first k-block to the owner of its last one, all of which hold
-                // work unless the phase has fewer pairs than CTAs (then warp 2
-                // lists the ones that do)
-                const bool every = ph.total >= G;
-                const int cf = owner_of((int64_t)mt * ph.nkb, ph.total, G);
-                const int cl = owner_of((int64_t)mt * ph.nkb + ph.nkb - 1, ph.total, G);
-                if (!every && warp == 2) {
+            // segments of tile mt of phase phx in k order: the CTAs from the
+            // owner of its first k-block to the owner of its last one, all of
+            // which hold work unless the phase has fewer pairs than CTAs (then
+            // warp 2 lists the ones that do into list / seg_info[info])
+            auto seg_list = [&](const Phase& phx, int mt_, int* list, int info, int& cf_, bool& every_) {
+                every_ = phx.total >= G;
+                cf_ = owner_of((int64_t)mt_ * phx.nkb, phx.total, G);
+                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1, phx.total, G);
+                if (!every_ && warp == 2) {
                     int n = 0, j = 0;
-                    for (int base = cf; base <= cl; base += 32) {
+                    for (int base = cf_; base <= cl_; base += 32) {
                         const int cc = base + lane;
-                        const bool w = cc <= cl && has_work(ph.total, G, cc);
+                        const bool w = cc <= cl_ && has_work(phx.total, G, cc);
                         const unsigned m = __ballot_sync(0xFFFFFFFFu, w);
-                        if (w) seg[n + __popc(m & ((1u << lane) - 1u))] = cc + mt;
+                        if (w) list[n + __popc(m & ((1u << lane) - 1u))] = cc + mt_;
                         n += __popc(m);
                         j += __popc(__ballot_sync(0xFFFFFFFFu, w && cc < cta));
                     }
-                    if (lane == 0) { seg_info[0] = n; seg_info[1] = j; }
+                    if (lane == 0) { seg_info[info] = n; seg_info[info + 1] = j; }
                 }
+                return cl_;
+            };
+            const Phase ph_o = merged ? phase_of(mp, p, k - 1) : ph;       // the o_proj phase of the layer
+            const size_t r1 = (size_t)(kFusedGridCap + p.max_mt);           // first slot of region 1
+            Units u2(ph, G, cta);
+            while (!(p.parallel && ph.kind == K_OPROJ) && u2.next(mt, kb0, kb1)) {
+                int cf, cf_o = 0;
+                bool every, every_o = true;
+                const int cl = seg_list(ph, mt, seg, 0, cf, every);
+                int cl_o = -1;
+                if (merged) cl_o = seg_list(ph_o, mt, seg2, 2, cf_o, every_o);
                 epi_sync();
-                const int nseg = every ? cl - cf + 1 : seg_info[0];
+                const int nseg_d = every ? cl - cf + 1 : seg_info[0];
                 const int jseg = every ? cta - cf : seg_info[1];
-                auto slot_of = [&](int j) { return every ? cf + j + mt : seg[j]; };
+                const int nseg_o = !merged ? 0 : (every_o ? cl_o - cf_o + 1 : seg_info[2]);
+                const int nseg = nseg_o + nseg_d;
+                // slot of segment j: the o_proj segments (region 1) first, then
+                // this phase's own, each in k order
+                auto slot_of = [&](int j) -> size_t {
+                    if (j < nseg_o) return r1 + (size_t)(every_o ? cf_o + j + mt : seg2[j]);
+                    const int jd = j - nseg_o;
+                    return (size_t)ph.region * r1 + (size_t)(every ? cf + jd + mt : seg[jd]);
+                };
+
                 // this CTA's share of the tile's tokens (none for most CTAs
                 // when B is small: those do not wait for the tile)
-                const int t_lo = (int)((int64_t)B * jseg / nseg), t_hi = (int)((int64_t)B * (jseg + 1) / nseg);
+                const int t_lo = (int)((int64_t)B * jseg / nseg_d), t_hi = (int)((int64_t)B * (jseg + 1) / nseg_d);
                 if (t_lo == t_hi) { epi_sync(); continue; }
                 if (leader && !dead &&
-                    !grid_wait(p.tickets + ph.kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort))
+                    !grid_wait(p.tickets + tk_kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort))
                     fail();
                 epi_sync();                     // every segment of the tile is visible
                 if (dead || *labort) { epi_sync(); continue; }
@@ -554,10 +600,10 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 // warp per token, lane per 4 consecutive rows; segments added
                 // in k order, all loads of a token issued before the sum
                 const int r0 = mt * 128 + lane * 4;
-                const __nv_bfloat16* resid = ph.kind == K_OPROJ
+                const __nv_bfloat16* resid = (ph.kind == K_OPROJ || merged)
                     ? (l == 0 ? p.x_in : (((l - 1) & 1) ? p.R1 : p.R0)) : p.h;
                 __nv_bfloat16* dst = ph.kind == K_OPROJ ? p.h : (l == p.L - 1 ? p.y_out : ((l & 1) ? p.R1 : p.R0));
-                const float* pbase = p.part + lane * 4;
+                const float* pbase = p.part + lane * 4;     // + slot * PART_FLOATS
                 const bool has_resid = ph.kind == K_OPROJ || ph.kind == K_DOWN;
                 auto emit = [&](int t, const float4& acc, const float4& acc2, const uint2& rv) {
                     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -664,14 +710,15 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 // after these stores, and then fences the async proxy)
                 epi_sync();                     // seg[] is rewritten for the next tile
             }
-            // This CTA's part of phase k is done (including its token shares).
-            // The counter counts completions of all phases, so a CTA signals
-            // phase k only once barrier k has passed (a CTA with no work in a
-            // phase gets here without having waited for it): then
-            // bar >= G (k+1) means that every CTA has finished phases 0..k.
+            // This CTA's part of phase k is done (including its token shares);
+            // after the last phase of a stage it signals the stage.  The
+            // counter counts completions of all stages, so a CTA signals stage
+            // s only once barrier s has passed (a CTA with no work in a stage
+            // gets here without having waited for it): then bar >= G (s+1)
+            // means that every CTA has finished stages 0..s.
             epi_sync();
-            if (leader && !dead) {
-                if (grid_wait(p.bar, (unsigned)G * (unsigned)k, labort, gabort)) {
+            if (ph.last_of_stage && leader && !dead) {
+                if (grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) {
                     red_release_add(p.bar, 1u);
                 } else {
                     fail();
@@ -731,7 +778,8 @@ FusedPlan plan_fused(const FusedShape& s) {
     f.h_off = o; o += up256((size_t)s.B * s.D * 2);
     f.hid_off = o; o += up256((size_t)s.B * s.F * 2);
     f.qkv_off = o; o += up256((size_t)s.tp * s.B * w_s * 2);
-    f.part_off = o; o += up256((size_t)(kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
+    // two regions of partial slots (the parallel block runs two phases per stage)
+    f.part_off = o; o += up256((size_t)2 * (kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
     f.total = o;
     return f;
 }
@@ -764,7 +812,7 @@ size_t fused_stack_ws_bytes(const FusedShape& s) { return plan_fused(s).total; }
 
 cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, const void* const* Wqkv,
                                const void* const* Wo, const void* const* Wg, const void* const* Wu,
-                               const void* const* Wd, int n_layers, void* ws, cudaStream_t st) {
+                               const void* const* Wd, int n_layers, bool parallel, void* ws, cudaStream_t st) {
     const FusedPlan f = plan_fused(s);
     const DeviceCtx* ctx = device_ctx();
     if (!ctx) return cudaErrorNoDevice;
@@ -794,6 +842,7 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
 
     FusedParams prm{};
     prm.B = (int)s.B; prm.D = (int)s.D; prm.F = (int)s.F; prm.G = G;
+    prm.parallel = parallel ? 1 : 0;
     prm.n_qkv = (int)n_qkv; prm.ko = (int)ko; prm.max_mt = f.max_mt; prm.eps = kRmsEpsilon;
     const int kv_s = s.tp <= s.n_kv ? s.n_kv / s.tp : 1;
     prm.qkv.n_q = s.n_q; prm.qkv.n_kv = s.n_kv; prm.qkv.head_dim = s.hd; prm.qkv.tp = s.tp;

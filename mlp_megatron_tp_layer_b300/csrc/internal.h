@@ -152,8 +152,9 @@ struct FusedShape {
 bool fused_stack_shape_ok(const FusedShape& s);
 size_t fused_stack_ws_bytes(const FusedShape& s);
 // The whole stack in persistent cooperative launches (kFusedMaxLayers layers each).
+// parallel: the parallel (PaLM) block y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)).
 cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, const void* const* Wqkv,
                                const void* const* Wo, const void* const* Wg, const void* const* Wu,
-                               const void* const* Wd, int n_layers, void* ws, cudaStream_t st);
+                               const void* const* Wd, int n_layers, bool parallel, void* ws, cudaStream_t st);
 
 }  // namespace tpl

@@ -399,6 +399,23 @@ def decoder_layer(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, shard
     return y
 
 
+def decoder_layer_parallel(x, W: dict, n_q: int, n_kv: int, head_dim: int, tp: int, trace: list | None = None):
+    """The parallel (PaLM) block of [L4] S5.5: y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)).
+
+    Both sublayers read the same normalised input, and their shard partials are
+    summed together in one reduction (the shared all-reduce of S5.5); the
+    residual stream is rounded to bf16 once per layer.  ``trace`` as in
+    decoder_layer, with y only.
+    """
+    xn = rmsnorm(x)
+    _, _, _, Pa = attn_proj_sharded(xn, W["Wqkv"], W["Wo"], n_q, n_kv, head_dim, tp)
+    _, Pm, _ = mlp_sharded(xn, W["Wg"], W["Wu"], W["Wd"], tp, bf16=True)
+    y = bf16_round(_f64(x) + shard_reduce(Pa, False) + shard_reduce(Pm, False))
+    if trace is not None:
+        trace.append(y)
+    return y
+
+
 def linear_attn_sum(xn, W, n_q, n_kv, head_dim):
     """Unsharded attention sublayer output before any rounding of the sum."""
     QKV = bf16_round(linear(xn, W["Wqkv"]))
@@ -411,10 +428,14 @@ def linear_attn_sum(xn, W, n_q, n_kv, head_dim):
 
 
 def decoder_stack(x, layers: list, n_q: int, n_kv: int, head_dim: int, tp: int, sharded: bool = True,
-                  trace: list | None = None):
+                  trace: list | None = None, block: str = "serial"):
     """Layers applied in order; returns the final residual stream (bf16 values).
-    ``trace`` as in decoder_layer: every rounded residual-stream value, in order."""
+    ``trace`` as in decoder_layer: every rounded residual-stream value, in order.
+    ``block``: "serial" (pre-norm, attention then MLP) or "parallel" ([L4] S5.5)."""
     y = bf16_round(x)
     for W in layers:
-        y = decoder_layer(y, W, n_q, n_kv, head_dim, tp, sharded, trace)
+        if block == "parallel":
+            y = decoder_layer_parallel(y, W, n_q, n_kv, head_dim, tp, trace)
+        else:
+            y = decoder_layer(y, W, n_q, n_kv, head_dim, tp, sharded, trace)
     return y

@@ -83,3 +83,16 @@ def test_overlapping_output_is_rejected():
                                 ctypes.c_void_p(4 * base), ctypes.c_void_p(6 * base), None, 8, 256, 1024, 2, 1,
                                 1, ctypes.c_void_p(5 * base), 16, s)
     assert st == 5
+
+
+def test_decoder_stack_rejects_bad_path_and_block_before_any_launch():
+    """Path / block checks run before anything touches a device: the parallel
+    block exists only on the fused implementation."""
+    one = (ctypes.c_void_p * 1)(16)
+    fake = ctypes.c_void_p(256)
+    args = [fake, fake, one, one, one, one, one, 1, 8, 1536, 8960, 12, 2, 128, 2, fake, 1 << 30]
+    unsupported = 6
+    assert lib.tpl_tp_decoder_stack_ex(*args, tpl.PATH_UNFUSED, tpl.BLOCK_PARALLEL, None) == unsupported
+    assert lib.tpl_tp_decoder_stack_ex(*args, 7, tpl.BLOCK_SERIAL, None) == unsupported
+    assert lib.tpl_tp_decoder_stack_ex(*args, tpl.PATH_AUTO, 5, None) == unsupported
+    assert lib.tpl_tp_decoder_stack_path(*args, 9, None) == unsupported

@@ -92,6 +92,35 @@ def check_layers_against_oracle(x, y, layers, n_q, n_kv, hd, tp, rows, what):
         prev = y_ref
 
 
+@pytest.mark.parametrize("B", [8, 64])
+def test_qwen_parallel_block_stack(B):
+    """28 Qwen-shaped layers in the parallel arrangement ([L4] S5.5): every layer,
+    fed the oracle's own residual stream on sampled rows, matches the oracle's
+    next value; the stack equals its layer-by-layer composition."""
+    D, F, n_q, n_kv, hd, tp, L = QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"], QW["n_layers"]
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=0, layer=l, prefix="qwen", device="cuda")
+              for l in range(L)]
+    x = si.activations(B, D, seed=1, name=f"bench.x{B}", device="cuda")
+    par = dict(block=tpl.BLOCK_PARALLEL)
+    y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, **par)
+    z = x
+    for W in layers:
+        z = tpl.tp_decoder_stack(z, [W], n_q, n_kv, hd, tp, **par)
+    assert_equal(y, to_np(z), what="parallel stack vs layer-by-layer")
+    rows = sample_rows(B, 8, seed=B)
+    trace = []
+    O.decoder_stack(np64(x)[rows], [{k: np64(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                    trace=trace, block="parallel")
+    idx = torch.as_tensor(rows, device=x.device)
+    prev = O.bf16_round(np64(x)[rows])
+    for l, W in enumerate(layers):
+        inp = x.clone()
+        inp[idx] = torch.from_numpy(prev).to(device=x.device, dtype=x.dtype)
+        out = tpl.tp_decoder_stack(inp, [W], n_q, n_kv, hd, tp, **par)
+        assert_within(to_np(out)[rows], trace[l], stack_allowance([trace[l]], trace[l]), what=f"layer {l}")
+        prev = trace[l]
+
+
 @pytest.mark.parametrize("B", [1, 64])
 def test_qwen_decode_stack_as_benchmarked(B):
     """The benchmark's decode step: 28 layers through tp_decoder_stack."""

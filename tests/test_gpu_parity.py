@@ -257,3 +257,23 @@ def test_decoder_stack_fused_in_place_and_gqa_shapes(B):
     y = x.clone()
     tpl.tp_decoder_stack(y, layers, n_q, n_kv, hd, tp, out=y, path=tpl.PATH_FUSED)
     assert_within(y, ref, stack_allowance(trace, ref), what="in-place fused stack")
+
+
+# ------------------------------------------ parallel (PaLM) block, [L4] S5.5
+
+@pytest.mark.parametrize("B", [1, 5, 40, 128])
+def test_decoder_stack_parallel_block(B):
+    """y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)) through the fused stack, against
+    the oracle; one bf16 rounding of the residual stream per layer."""
+    D, F, n_q, n_kv, hd, tp, L = 256, 512, 4, 2, 64, 2, 3
+    x = si.activations(B, D, seed=9, device="cuda")
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=9, layer=l, sigma=0.05, device="cuda") for l in range(L)]
+    trace = []
+    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                          trace=trace, block="parallel")
+    y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, block=tpl.BLOCK_PARALLEL)
+    assert_within(y, ref, stack_allowance(trace, ref), what="parallel-block stack")
+    y1 = tpl.tp_decoder_stack(x, layers[:1], n_q, n_kv, hd, tp, block=tpl.BLOCK_PARALLEL)
+    assert_within(y1, trace[0], stack_allowance(trace[:1], trace[0]), what="first layer")
+    y2 = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, block=tpl.BLOCK_PARALLEL)
+    assert_equal(y2, to_np(y), what="second run")

@@ -380,6 +380,32 @@ def test_decoder_layer_zero_output_projections_is_identity():
     assert np.allclose(y, O.bf16_round(x + a), rtol=0, atol=2 ** -7 * np.abs(x + a).max())
 
 
+def test_parallel_block_reduces_to_its_sublayers():
+    """[L4] S5.5 parallel block: silencing one sublayer's output projection leaves
+    x plus the other sublayer on RMSNorm(x), each computed here without shards."""
+    r = rng(16)
+    D, F, n_q, n_kv, hd = 16, 32, 4, 2, 4
+    x = O.bf16_round(r.standard_normal((3, D)))
+    W = dict(Wqkv=r.standard_normal(((n_q + 2 * n_kv) * hd, D)) / 4, Wo=r.standard_normal((D, n_q * hd)) / 8,
+             Wg=r.standard_normal((F, D)) / 4, Wu=r.standard_normal((F, D)) / 4, Wd=r.standard_normal((D, F)) / 8)
+    xn = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + O.RMS_EPS)
+    attn, _ = O.attn_proj_unsharded(xn, W["Wqkv"], W["Wo"], n_q, n_kv, hd, bf16=True)
+    g, u = xn @ W["Wg"].T, xn @ W["Wu"].T
+    mlp = O.bf16_round(g / (1 + np.exp(-g)) * u) @ W["Wd"].T
+    tol = lambda ref: 2 ** -7 * np.abs(ref) + 1e-9   # noqa: E731  (one bf16 rounding, sum order)
+    W0 = dict(W, Wo=np.zeros_like(W["Wo"]))
+    ref = O.bf16_round(x + mlp)
+    assert np.all(np.abs(O.decoder_layer_parallel(x, W0, n_q, n_kv, hd, tp=2) - ref) <= tol(ref))
+    W1 = dict(W, Wd=np.zeros_like(W["Wd"]))
+    ref = O.bf16_round(x + attn)
+    assert np.all(np.abs(O.decoder_layer_parallel(x, W1, n_q, n_kv, hd, tp=2) - ref) <= tol(ref))
+    ref = O.bf16_round(x + attn + mlp)
+    assert np.all(np.abs(O.decoder_layer_parallel(x, W, n_q, n_kv, hd, tp=2) - ref) <= tol(ref))
+    # and it is not the serial block: there the MLP sees RMSNorm(x + attn)
+    assert np.abs(O.decoder_layer_parallel(x, W, n_q, n_kv, hd, tp=2)
+                  - O.decoder_layer(x, W, n_q, n_kv, hd, tp=2)).max() > 1e-3
+
+
 def test_decoder_stack_sharded_matches_unsharded():
     r = rng(15)
     D, F, n_q, n_kv, hd = 32, 64, 8, 2, 4
