@@ -62,7 +62,10 @@ def args_parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-llama", action="store_true", help="skip the Llama-3.1-70B-shaped decode stack")
     ap.add_argument("--no-cases", action="store_true", help="skip the sharded-matmul cases and shard_reduce")
-    ap.add_argument("--only", choices=["decode", "prefill", "llama"], default=None,
+    ap.add_argument("--no-lm-head", action="store_true", help="skip the vocabulary-parallel lm_head lines")
+    ap.add_argument("--lm-head-model", choices=["llama-3.1-70b", "qwen2.5-1.5b"], default=None,
+                    help="with --only lm_head: one model's shape only (--batches selects the batch sizes)")
+    ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
     ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
@@ -491,6 +494,62 @@ def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     return out
 
 
+# Vocabulary-parallel lm_head shapes: the models' vocabularies and hidden sizes
+# with the TP degree of their decode configurations.
+LM_HEADS = {
+    "llama-3.1-70b": {"D": 8192, "V": 128256, "tp": 8, "batches": (1, 8, 64, 128)},
+    "qwen2.5-1.5b": {"D": 1536, "V": 151936, "tp": 2, "batches": (1, 8, 32, 64)},
+}
+
+
+def run_lm_head(args, tpl, dev, peaks, stream, k=1):
+    """Greedy next-token selection through the vocabulary-parallel lm_head:
+    per-shard top-k in the GEMM epilogue, then the candidate exchange.  One
+    graph-replayed call per batch size; GB/s counts the weight and input bytes
+    (V*D*2 + B*D*2), the logits never being written."""
+    out = {}
+    reps = max(5, args.steps // 2)
+    for name, c in LM_HEADS.items():
+        if args.only == "lm_head" and args.lm_head_model not in (None, name):
+            continue
+        D, V, tp = c["D"], c["V"], c["tp"]
+        batches = c["batches"]
+        if args.only == "lm_head" and args.batches:
+            batches = tuple(int(b) for b in args.batches.split(","))
+        x_all, W = si.lm_head(max(batches), D, V, seed=0, device=dev)
+        res = {"workload": f"{name}-shaped lm_head: W[{V}, {D}] bf16 ({V * D * 2 / 1e9:.2f} GB), "
+                           f"TP={tp} vocabulary shards, top-{k} per shard then exchange",
+               "per_batch": {}}
+        for B in batches:
+            x = x_all[:B].contiguous()
+            idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+            val = torch.empty(B, k, dtype=torch.float32, device=dev)
+            ws = tpl.workspace(tpl.vocab_topk_workspace_bytes(B, V, tp, k), dev)
+            with torch.cuda.stream(stream):
+                tpl.vocab_parallel_topk(x, W, tp, k, out=(idx, val), ws=ws)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                tpl.vocab_parallel_topk(x, W, tp, k, out=(idx, val), ws=ws)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b) / reps
+            gbs = (V * D * 2 + B * D * 2) / (t / 1e3) / 1e9
+            res["per_batch"][str(B)] = {"ms": t, "GB/s": gbs, "frac_of_peak": gbs / peaks["hbm_gbs"]}
+            del g
+        out[name] = res
+        del x_all, W
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_ms(fn, reps):
     """Average device time of fn over reps calls (CUDA events, after 3 warm-up calls)."""
     for _ in range(3):
@@ -594,6 +653,11 @@ def main():
             print(json.dumps(dict(pre, metric=METRIC, n_gpus=world, steps=args.steps, warmup=args.warmup)),
                   flush=True)
         return
+    if args.only == "lm_head":
+        lm = run_lm_head(args, tpl, dev, peaks, stream)
+        if rank == 0:
+            print(json.dumps(dict(lm_head=lm, metric=METRIC, n_gpus=world, steps=args.steps)), flush=True)
+        return
     if args.only == "llama":
         ll = run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream)
         if rank == 0:
@@ -610,6 +674,10 @@ def main():
     prefill = None
     if not args.no_prefill and args.only is None:
         prefill = run_prefill(args, tpl, dev, world, peaks, peak_kind, stream)
+
+    lm_head = None
+    if not args.no_lm_head and args.only is None:
+        lm_head = run_lm_head(args, tpl, dev, peaks, stream)
 
     cases = reduce_line = None
     if not args.no_cases and args.only is None:
@@ -634,7 +702,8 @@ def main():
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
                 "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"],
                 "qwen_decode_parallel_block": parallel, "llama_decode": llama,
-                "prefill": prefill, "sharded_matmul": cases, "shard_reduce": reduce_line}
+                "prefill": prefill, "lm_head_topk": lm_head, "sharded_matmul": cases,
+                "shard_reduce": reduce_line}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -279,6 +279,39 @@ tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void* const* Wq
                                    void* stream);
 
 /* --------------------------------------------------------------------------
+ * Vocabulary-parallel lm_head with a top-k candidate exchange
+ * ("Lecture 4 - Distributed Serving", S4.5 "lm_head and sequence parallelism").
+ * The lm_head is split by vocabulary: shard s owns the rows
+ * [s V/tp, (s+1) V/tp) of W and scores only those entries.  Instead of
+ * gathering all V logits per token, each shard keeps its k best (index, logit)
+ * pairs and only those tp x k candidates per token are exchanged; the result
+ * is the global top-k of the logits x . W[v].
+ *   X          [B, D] bf16 row-major: final hidden states (after any final
+ *              norm; a positive per-token scale does not change the ranking).
+ *   W          [V, D] bf16 row-major: lm_head weight, one row per vocabulary
+ *              entry ([out, in]).  Read only.
+ *   top_idx    [B, k] int32 out: vocabulary indices, best first.
+ *   top_val    [B, k] fp32 out, may be NULL: their logits (fp32 accumulation
+ *              of the bf16 products).
+ *   shard_idx, shard_val  [tp, B, k] out, each may be NULL: every shard's own
+ *              top-k, i.e. the candidates that are exchanged.
+ * Order: larger logit first; equal logits (-0 equals +0) by lower index, so
+ * the result is unique and deterministic.  NaN logits rank above +inf.
+ * Requires 1 <= B, V % tp == 0, 1 <= k <= min(8, V / tp), D % 8 == 0
+ * (TPL_ERR_SHAPE), V < 2^31, dtype TPL_BF16 (TPL_ERR_DTYPE), X and W 16-byte
+ * aligned, outputs 4-byte aligned (TPL_ERR_ALIGN), outputs disjoint from the
+ * inputs and the workspace (TPL_ERR_ALIAS), ws of at least the size
+ * tpl_vocab_parallel_topk_workspace reports (TPL_ERR_WORKSPACE; nothing in it
+ * needs to start at zero), and the sm_103 tensor-core path
+ * (TPL_ERR_UNSUPPORTED otherwise).  Two kernels on `stream`; asynchronous.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_vocab_parallel_topk_workspace(int64_t B, int64_t V, int tp, int k, size_t* bytes);
+tpl_status tpl_vocab_parallel_topk(const void* X, const void* W, int64_t B, int64_t D, int64_t V,
+                                   int tp, int k, int dtype, int32_t* top_idx, float* top_val,
+                                   int32_t* shard_idx, float* shard_val, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * Launch timing, for measurement only (off by default).
  * tpl_profile_enable(n > 0) creates n pairs of CUDA events (host objects; no
  * device memory) and from then on brackets each kernel launch with a pair on

@@ -62,6 +62,9 @@ _SIGS = {
     "tpl_tp_decoder_stack": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                     ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
                                     _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tpl_vocab_parallel_topk_workspace": (_i32, [_i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tpl_vocab_parallel_topk": (_i32, [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                       _sz, _vp]),
 }
 
 
@@ -370,3 +373,41 @@ def profile_records():
         _check(lib.tpl_profile_read(i, buf, 64, ctypes.byref(ms)), "tpl_profile_read")
         out.append((buf.value.decode(), float(ms.value)))
     return out
+
+
+def vocab_topk_workspace_bytes(B, V, tp, k) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_vocab_parallel_topk_workspace(B, V, tp, k, ctypes.byref(n)),
+           "tpl_vocab_parallel_topk_workspace")
+    return n.value
+
+
+def vocab_parallel_topk(x, W, tp: int, k: int = 1, shard_outputs: bool = False, out=None, ws=None,
+                        stream=None):
+    """Top-k next-token candidates of the vocabulary-parallel lm_head.
+
+    x [B, D] and W [V, D] bf16; shard s owns rows [s V/tp, (s+1) V/tp) of W.
+    Returns (idx [B, k] int32, val [B, k] fp32); with ``shard_outputs`` also
+    each shard's own top-k (sidx, sval), both [tp, B, k].  ``out`` may supply
+    the (idx, val) tensors."""
+    _contig(x, W)
+    B, D = x.shape
+    V = W.shape[0]
+    if W.shape[1] != D:
+        raise ValueError("W must be [V, D]")
+    dev = x.device
+    if out is None:
+        idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+        val = torch.empty(B, k, dtype=torch.float32, device=dev)
+    else:
+        idx, val = out
+    sidx = sval = None
+    if shard_outputs:
+        sidx = torch.empty(tp, B, k, dtype=torch.int32, device=dev)
+        sval = torch.empty(tp, B, k, dtype=torch.float32, device=dev)
+    nbytes = vocab_topk_workspace_bytes(B, V, tp, k)
+    ws = workspace(nbytes, dev) if ws is None else ws
+    _check(lib.tpl_vocab_parallel_topk(_p(x), _p(W), B, D, V, tp, k, _dt(x), _p(idx), _p(val), _p(sidx), _p(sval),
+                                       _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpl_vocab_parallel_topk")
+    return (idx, val, sidx, sval) if shard_outputs else (idx, val)

@@ -755,6 +755,61 @@ extern "C" tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* W
     return tpl_tp_decoder_stack(x, y, q, o, g, u, d, 1, B, D, F, n_q, n_kv, head_dim, tp, ws, ws_bytes, stream);
 }
 
+// ----------------------------------------------- vocabulary-parallel lm_head
+
+namespace {
+tpl_status check_vocab_shape(int64_t B, int64_t V, int tp, int k) {
+    if (B < 1 || V < 1 || tp < 1 || V % tp != 0 || V >= (int64_t(1) << 31)) return TPL_ERR_SHAPE;
+    if (k < 1 || k > kVocabTopkMax || k > V / tp) return TPL_ERR_SHAPE;
+    if (B > 65535 * int64_t(1024)) return TPL_ERR_SHAPE;
+    return TPL_OK;
+}
+bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+}  // namespace
+
+extern "C" tpl_status tpl_vocab_parallel_topk_workspace(int64_t B, int64_t V, int tp, int k, size_t* bytes) {
+    if (!bytes) return TPL_ERR_NULL;
+    const tpl_status s = check_vocab_shape(B, V, tp, k);
+    if (s != TPL_OK) return s;
+    *bytes = vocab_topk_ws_bytes(B, V, tp, k);
+    return TPL_OK;
+}
+
+extern "C" tpl_status tpl_vocab_parallel_topk(const void* X, const void* W, int64_t B, int64_t D, int64_t V,
+                                              int tp, int k, int dtype, int32_t* top_idx, float* top_val,
+                                              int32_t* shard_idx, float* shard_val, void* ws, size_t ws_bytes,
+                                              void* stream) {
+    if (!X || !W || !top_idx) return TPL_ERR_NULL;
+    tpl_status s = check_vocab_shape(B, V, tp, k);
+    if (s != TPL_OK) return s;
+    if (D < 8 || D % 8 != 0) return TPL_ERR_SHAPE;
+    if (dtype != TPL_BF16) return TPL_ERR_DTYPE;
+    if (!al16(X) || !al16(W) || !al4(top_idx) || (top_val && !al4(top_val)) || (shard_idx && !al4(shard_idx)) ||
+        (shard_val && !al4(shard_val)))
+        return TPL_ERR_ALIGN;
+    const size_t need = vocab_topk_ws_bytes(B, V, tp, k);
+    if (!ws || ws_bytes < need) return TPL_ERR_WORKSPACE;
+    if (!al16(ws)) return TPL_ERR_ALIGN;
+    const size_t xb = (size_t)B * D * 2, wb = (size_t)V * D * 2;
+    const size_t ob = (size_t)B * k * 4, sb = (size_t)tp * B * k * 4;
+    const void* outs[4] = {top_idx, top_val, shard_idx, shard_val};
+    const size_t osz[4] = {ob, ob, sb, sb};
+    for (int i = 0; i < 4; ++i) {
+        if (!outs[i]) continue;
+        if (overlap(outs[i], osz[i], X, xb) || overlap(outs[i], osz[i], W, wb) || overlap(outs[i], osz[i], ws, need))
+            return TPL_ERR_ALIAS;
+        for (int j = 0; j < i; ++j)
+            if (outs[j] && overlap(outs[i], osz[i], outs[j], osz[j])) return TPL_ERR_ALIAS;
+    }
+    if (overlap(ws, need, X, xb) || overlap(ws, need, W, wb)) return TPL_ERR_ALIAS;
+    if (!device_ctx()) return TPL_ERR_CUDA;
+    if (!tc_gemm_supported()) return TPL_ERR_UNSUPPORTED;
+    VocabTopkArgs a{X, W, B, D, V, tp, k, top_idx, top_val, shard_idx, shard_val, ws};
+    cudaStream_t st = S(stream);
+    ProfScope prof("lm_head_topk", st);
+    return cuda_status(launch_vocab_topk(a, st));
+}
+
 extern "C" tpl_status tpl_profile_enable(int max_launches) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     for (auto& p : g_prof) {

@@ -139,6 +139,24 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st);
 // 64 columns x box_rows rows, 128-byte swizzle; cached per argument tuple.
 bool tma_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
 
+// ------------------------------------------------ vocabulary-parallel lm_head
+constexpr int kVocabTopkMax = 8;      // largest k of the candidate exchange
+
+struct VocabTopkArgs {
+    const void* X;          // [B, D] bf16 final hidden states
+    const void* W;          // [V, D] bf16 lm_head weight, shard s = rows [s V/tp, (s+1) V/tp)
+    int64_t B, D, V;
+    int tp, k;
+    int32_t* top_idx;       // [B, k]
+    float* top_val;         // [B, k] or null
+    int32_t* shard_idx;     // [tp, B, k] or null
+    float* shard_val;       // [tp, B, k] or null
+    void* ws;               // vocab_topk_ws_bytes(B, V, tp, k), 256-byte aligned
+};
+size_t vocab_topk_ws_bytes(int64_t B, int64_t V, int tp, int k);
+// The GEMM + per-tile ranking kernel, then the per-shard / exchange merge kernel.
+cudaError_t launch_vocab_topk(const VocabTopkArgs& a, cudaStream_t st);
+
 // ------------------------------------------------ fused decode stack
 constexpr float kRmsEpsilon = 1e-6f;  // RMSNorm eps of the decoder composition
 constexpr int kFusedMaxLayers = 32;   // layers per launch (longer stacks take several launches)

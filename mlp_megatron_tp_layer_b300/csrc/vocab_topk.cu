@@ -1,0 +1,471 @@
+// Vocabulary-parallel lm_head with a candidate exchange instead of a logit
+// gather ("Lecture 4 - Distributed Serving", S4.5): shard s owns the vocabulary
+// rows [s V/tp, (s+1) V/tp) of W[V, D]; it ranks only its own logits
+// x . W[v] and keeps its top-k, and the tp shard lists per token are merged
+// into the global top-k.  The logits themselves never reach HBM.
+//
+// Kernel 1 (vocab_topk_gemm_kernel): persistent TMA + tcgen05 GEMM in the
+// swapped orientation -- 128 vocabulary rows of W are the M operand, the
+// tokens (padded to N = 16..128 by the TMA zero fill) the N operand -- so W
+// streams from HBM once per call for B <= 128.  Tiles never straddle a shard:
+// the tile list is shard-major and a shard's last tile masks the rows past its
+// end.  The epilogue ranks each tile's 128 logits per token: each epilogue
+// warp takes its 32 rows by repeated warp max (redux.sync) over an
+// order-preserving integer key, the four warps' lists are merged through
+// shared memory, and the tile's k best candidates per token go to global
+// memory as packed 64-bit words.
+//
+// Kernel 2 (vocab_topk_merge_kernel): one block per (token, shard) reduces
+// that shard's tile candidates to the shard's top-k (the list a device would
+// send); the last block of each token to finish (an atomic ticket, no
+// waiting) merges the tp shard lists into the final top-k.
+//
+// Candidate word: (order key of the fp32 logit) << 32 | (0xFFFFFFFF - index).
+// Comparing words as unsigned integers orders by logit, larger first, and
+// equal logits by lower vocabulary index; 0 marks an empty slot.  -0 is
+// turned into +0 before keying, so the two compare equal.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpl {
+namespace {
+
+constexpr int VT_BM = 128;          // vocabulary rows per tile (TMEM lanes)
+constexpr int VT_BK = 64;           // K elements per stage (one 128-byte swizzle row)
+constexpr int VT_THREADS = 192;     // warp 0 TMA, warp 1 TMEM + MMA, warps 2..5 epilogue
+constexpr int VT_MERGE_THREADS = 256;
+
+struct VtParams {
+    int64_t B;              // tokens
+    int64_t Vs;             // vocabulary rows per shard
+    int k;                  // candidates kept per (tile or shard, token)
+    int tiles_per_shard;    // ceil(Vs / 128)
+    int m_tiles;            // tp * tiles_per_shard
+    int64_t total_tiles;    // m_tiles * token tiles
+    int nkb;                // ceil(D / 64)
+    unsigned long long* cand;   // [m_tiles][B][k]
+    unsigned int* tickets;      // [B], zeroed here for the merge kernel
+    int n_tickets;
+    unsigned int* err;
+};
+
+template <int BN>
+struct VtCfg {
+    static constexpr int A_BYTES = VT_BM * VT_BK * 2;               // 16 KB of W
+    static constexpr int B_BYTES = BN * VT_BK * 2;                  // tokens
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
+    static constexpr int CH = BN >= 32 ? 32 : 16;                    // columns per TMEM load
+    static constexpr int CAND_BYTES = 4 * CH * kVocabTopkMax * 8;   // four warps' lists per column
+    static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CAND_BYTES + 256 + 1024;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile must be 16..128 in steps of 16");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    if (f == 0.0f) f = 0.0f;                                          // -0 ranks with +0
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return key > 1u ? key : 1u;                                       // 0 is reserved for "empty"
+}
+__device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t index) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - index);
+}
+__device__ __forceinline__ void unpack(unsigned long long w, int32_t& index, float& value) {
+    if (w == 0ull) { index = -1; value = __uint_as_float(0xFF800000u); return; }
+    const uint32_t key = (uint32_t)(w >> 32);
+    index = (int32_t)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
+    value = __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// bar.sync / bar.red over the four epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_all(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "setp.ne.u32 a, %1, 0;\n\t"
+        "bar.red.and.pred b, 1, 128, a;\n\t"
+        "selp.u32 %0, 1, 0, b;\n\t}"
+        : "=r"(r) : "r"((uint32_t)p) : "memory");
+    return r != 0;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(VT_THREADS, 1)
+vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const VtParams p) {
+    using C = VtCfg<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::CAND_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* acc_full = bars + 2 * C::STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the merge kernel that follows on the stream counts finished shards here
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&acc_full[a]), 1);
+            mbar_init(smem_addr(&acc_empty[a]), 4);
+        }
+        mbar_init(smem_addr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.err) atomicOr(p.err, TPL_DEVERR_TIMEOUT);
+    };
+    // tile t -> (shard-major vocabulary tile, token tile)
+    auto w_row = [&](int64_t t) {
+        const int mg = (int)(t % p.m_tiles);
+        const int s = mg / p.tiles_per_shard, lt = mg - s * p.tiles_per_shard;
+        return (int)(s * p.Vs + (int64_t)lt * VT_BM);
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_tail = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                const int wr = w_row(t);
+                const int xr = (int)(t / p.m_tiles) * BN;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(smem_addr(&empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    mbar_expect_tx(fb, C::STAGE_BYTES);
+                    uint8_t* st = smem + stage * C::STAGE_BYTES;
+                    tma_load_hint(smem_addr(st), &tmW, fb, kb * VT_BK, wr, pol_w);
+                    tma_load_hint(smem_addr(st + C::A_BYTES), &tmX, fb, kb * VT_BK, xr, pol_x);
+                    issued_tail = min(issued_tail + 1, C::STAGES);
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                fail();
+                for (int i = 0; i < issued_tail; ++i) {
+                    if (--stage < 0) { stage = C::STAGES - 1; phase ^= 1; }
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_addr(&full[stage]), phase) && globaltimer() - t0 < kWaitLimitNs) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(VT_BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(smem_addr(&full[stage]), phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * C::STAGE_BYTES);
+                    const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < VT_BK / 16; ++kk)
+                        mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+                    mma_commit(smem_addr(&empty[stage]));
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_addr(&acc_full[acc]));
+            }
+            if (!ok) fail();
+            mma_commit(smem_addr(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_addr(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {}
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lanes 32q..32q+31 = tile rows
+        const int et = threadIdx.x - 64;        // 0..127 across the four epilogue warps
+        const int k = p.k;
+        int it = 0;
+        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            // the four warps leave together, so the named barriers below never
+            // wait for a warp that has given up
+            const bool ok = epi_all(mbar_wait(smem_addr(&acc_full[acc]), acc_phase, abort_flag));
+            if (!ok) { if (et == 0) fail(); break; }
+            tc_fence_after();
+            const int mg = (int)(t % p.m_tiles);
+            const int s = mg / p.tiles_per_shard, lt = mg - s * p.tiles_per_shard;
+            const int64_t tok0 = (t / p.m_tiles) * BN;
+            const int64_t local0 = (int64_t)lt * VT_BM + q * 32;           // shard-local row of lane 0
+            const bool row_ok = local0 + lane < p.Vs;
+            const uint32_t vbase = (uint32_t)(s * p.Vs + local0);           // vocabulary index of lane 0
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            float v[32];
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+                if (C::CH == 32) tmem_ld32(tbase + c0, v); else tmem_ld16(tbase + c0, v);
+                if (c0 + C::CH >= BN) {            // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&acc_empty[acc]));
+                }
+                // this warp's 32 rows: k rounds of warp max per token column
+#pragma unroll
+                for (int j = 0; j < C::CH; ++j) {
+                    const bool live = row_ok && tok0 + c0 + j < p.B;
+                    uint32_t key = live ? order_key(v[j]) : 0u;
+                    unsigned long long* dst = s_cand + (q * C::CH + j) * kVocabTopkMax;
+                    for (int i = 0; i < k; ++i) {
+                        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key);
+                        if (m == 0u) {
+                            if (lane == 0) for (int r = i; r < k; ++r) dst[r] = 0ull;
+                            break;
+                        }
+                        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, key == m);
+                        const int l = __ffs(hit) - 1;                // lowest row among equal logits
+                        if (lane == 0) dst[i] = pack(m, vbase + l);
+                        if (lane == l) key = 0u;
+                    }
+                }
+                epi_sync();
+                // merge the four sorted lists of one token column per thread
+                if (et < C::CH && tok0 + c0 + et < p.B) {
+                    unsigned long long* out = p.cand + ((int64_t)mg * p.B + tok0 + c0 + et) * k;
+                    const unsigned long long* src = s_cand + et * kVocabTopkMax;
+                    int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+                    for (int i = 0; i < k; ++i) {
+                        const unsigned long long c0w = h0 < k ? src[(0 * C::CH) * kVocabTopkMax + h0] : 0ull;
+                        const unsigned long long c1w = h1 < k ? src[(1 * C::CH) * kVocabTopkMax + h1] : 0ull;
+                        const unsigned long long c2w = h2 < k ? src[(2 * C::CH) * kVocabTopkMax + h2] : 0ull;
+                        const unsigned long long c3w = h3 < k ? src[(3 * C::CH) * kVocabTopkMax + h3] : 0ull;
+                        const unsigned long long a = c0w > c1w ? c0w : c1w;
+                        const unsigned long long b = c2w > c3w ? c2w : c3w;
+                        const unsigned long long best = a > b ? a : b;
+                        out[i] = best;
+                        if (best != 0ull) {
+                            if (best == c0w) ++h0;
+                            else if (best == c1w) ++h1;
+                            else if (best == c2w) ++h2;
+                            else ++h3;
+                        }
+                    }
+                }
+                epi_sync();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Insert w into the descending list L[0..kVocabTopkMax), dropping the smallest.
+__device__ __forceinline__ void list_insert(unsigned long long (&L)[kVocabTopkMax], unsigned long long w) {
+#pragma unroll
+    for (int i = 0; i < kVocabTopkMax; ++i) {
+        const unsigned long long hi = L[i] > w ? L[i] : w;
+        w = L[i] > w ? w : L[i];
+        L[i] = hi;
+    }
+}
+
+// Block-wide top-k of the union of the threads' descending lists: k rounds of
+// block max, the owner of each winner popping it.  Writes out[0..k) (shared).
+__device__ void block_topk(unsigned long long (&L)[kVocabTopkMax], int k, unsigned long long* out,
+                           unsigned long long* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int NW = VT_MERGE_THREADS / 32;
+    for (int i = 0; i < k; ++i) {
+        unsigned long long m = L[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            m = y > m ? y : m;
+        }
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long b = red[0];
+            for (int w = 1; w < NW; ++w) b = red[w] > b ? red[w] : b;
+            out[i] = b;
+        }
+        __syncthreads();
+        const unsigned long long win = out[i];
+        if (win != 0ull && L[0] == win) {            // words are unique, so one owner
+#pragma unroll
+            for (int j = 0; j + 1 < kVocabTopkMax; ++j) L[j] = L[j + 1];
+            L[kVocabTopkMax - 1] = 0ull;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(VT_MERGE_THREADS)
+vocab_topk_merge_kernel(const unsigned long long* __restrict__ cand, unsigned long long* shard_best,
+                        unsigned int* tickets, int64_t B, int tp, int tiles_per_shard, int k, int32_t* top_idx,
+                        float* top_val, int32_t* shard_idx, float* shard_val) {
+    __shared__ unsigned long long s_out[kVocabTopkMax];
+    __shared__ unsigned long long s_red[VT_MERGE_THREADS / 32];
+    __shared__ int s_last;
+    const int64_t b = blockIdx.x;
+    const int s = blockIdx.y;
+
+    // this shard's top-k for token b: the "local maximum / top-k" of one device
+    unsigned long long L[kVocabTopkMax];
+#pragma unroll
+    for (int i = 0; i < kVocabTopkMax; ++i) L[i] = 0ull;
+    const int n = tiles_per_shard * k;
+    for (int c = threadIdx.x; c < n; c += VT_MERGE_THREADS) {
+        const int lt = c / k, i = c - lt * k;
+        list_insert(L, cand[(((int64_t)s * tiles_per_shard + lt) * B + b) * k + i]);
+    }
+    block_topk(L, k, s_out, s_red);
+    if (threadIdx.x < k) {
+        const unsigned long long w = s_out[threadIdx.x];
+        shard_best[((int64_t)s * B + b) * k + threadIdx.x] = w;
+        if (shard_idx || shard_val) {
+            int32_t ix;
+            float val;
+            unpack(w, ix, val);
+            if (shard_idx) shard_idx[((int64_t)s * B + b) * k + threadIdx.x] = ix;
+            if (shard_val) shard_val[((int64_t)s * B + b) * k + threadIdx.x] = val;
+        }
+    }
+
+    // exchange: the last shard of token b to finish merges the tp lists
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&tickets[b], 1u) == (unsigned)(tp - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < kVocabTopkMax; ++i) L[i] = 0ull;
+    for (int c = threadIdx.x; c < tp * k; c += VT_MERGE_THREADS) {
+        const int ss = c / k, i = c - ss * k;
+        list_insert(L, __ldcg(shard_best + ((int64_t)ss * B + b) * k + i));
+    }
+    block_topk(L, k, s_out, s_red);
+    if (threadIdx.x < k) {
+        int32_t ix;
+        float val;
+        unpack(s_out[threadIdx.x], ix, val);
+        top_idx[b * k + threadIdx.x] = ix;
+        if (top_val) top_val[b * k + threadIdx.x] = val;
+    }
+}
+
+template <int BN>
+cudaError_t launch_bn(const VocabTopkArgs& a, const VtParams& p0, cudaStream_t st) {
+    using C = VtCfg<BN>;
+    const DeviceCtx* ctx = device_ctx();
+    if (!ctx) return cudaErrorNoDevice;
+    static bool attr_set[64] = {};
+    if (ctx->device < 64 && !attr_set[ctx->device]) {
+        const cudaError_t e = cudaFuncSetAttribute(vocab_topk_gemm_kernel<BN>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[ctx->device] = true;
+    }
+    CUtensorMap mW, mX;
+    if (!tma_map_bf16(&mW, a.W, a.V, a.D, a.D, VT_BM)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mX, a.X, a.B, a.D, a.D, BN)) return cudaErrorInvalidValue;
+    VtParams p = p0;
+    const int64_t n_tiles = (a.B + BN - 1) / BN;
+    p.total_tiles = (int64_t)p.m_tiles * n_tiles;
+    p.err = ctx->err_word;
+    const int64_t grid = std::min<int64_t>(p.total_tiles, ctx->num_sms);
+    vocab_topk_gemm_kernel<BN><<<(unsigned)grid, VT_THREADS, C::SMEM_BYTES, st>>>(mW, mX, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t vocab_topk_ws_bytes(int64_t B, int64_t V, int tp, int k) {
+    const int64_t tps = (V / tp + VT_BM - 1) / VT_BM;
+    const size_t cand = (size_t)tp * tps * B * k * 8;
+    const size_t shard = (size_t)tp * B * k * 8;
+    const size_t tick = (size_t)B * 4;
+    auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+    return up(cand) + up(shard) + up(tick);
+}
+
+cudaError_t launch_vocab_topk(const VocabTopkArgs& a, cudaStream_t st) {
+    const int64_t Vs = a.V / a.tp;
+    const int64_t tps = (Vs + VT_BM - 1) / VT_BM;
+    auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(ws);
+    unsigned long long* shard_best =
+        reinterpret_cast<unsigned long long*>(ws + up((size_t)a.tp * tps * a.B * a.k * 8));
+    unsigned int* tickets = reinterpret_cast<unsigned int*>(
+        reinterpret_cast<uint8_t*>(shard_best) + up((size_t)a.tp * a.B * a.k * 8));
+
+    VtParams p{};
+    p.B = a.B;
+    p.Vs = Vs;
+    p.k = a.k;
+    p.tiles_per_shard = (int)tps;
+    p.m_tiles = (int)(a.tp * tps);
+    p.nkb = (int)((a.D + VT_BK - 1) / VT_BK);
+    p.cand = cand;
+    p.tickets = tickets;
+    p.n_tickets = (int)a.B;
+    cudaError_t e;
+    if (a.B <= 16) e = launch_bn<16>(a, p, st);
+    else if (a.B <= 32) e = launch_bn<32>(a, p, st);
+    else if (a.B <= 64) e = launch_bn<64>(a, p, st);
+    else e = launch_bn<128>(a, p, st);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)a.B, (unsigned)a.tp);
+    vocab_topk_merge_kernel<<<grid, VT_MERGE_THREADS, 0, st>>>(cand, shard_best, tickets, a.B, a.tp, (int)tps, a.k,
+                                                               a.top_idx, a.top_val, a.shard_idx, a.shard_val);
+    return cudaGetLastError();
+}
+
+}  // namespace tpl

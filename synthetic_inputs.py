@@ -169,6 +169,13 @@ def activations(B, D, seed=0, name="X", device="cpu", dtype=torch.bfloat16):
     return normal((B, D), 1.0, seed, name, dtype, device)
 
 
+def lm_head(B, D, V, seed=0, device="cpu", dtype=torch.bfloat16, sigma=0.02):
+    """Final hidden states x[B, D] ~ N(0,1) (unit rms, as after the final
+    RMSNorm) and an lm_head weight W[V, D] ~ N(0, sigma^2)."""
+    return (normal((B, D), 1.0, seed, "lm_head.x", dtype, device),
+            normal((V, D), sigma, seed, "lm_head.W", dtype, device))
+
+
 def sharded_case_operands(I, J, K, seed=0, device="cpu", dtype=torch.bfloat16):
     """A[I,J] ~ N(0,1) and B[J,K] ~ N(0,1)/sqrt(J), B stored transposed as Bt[K,J]."""
     return dict(A=normal((I, J), 1.0, seed, "cases.A", dtype, device),

@@ -96,3 +96,30 @@ def test_decoder_stack_rejects_bad_path_and_block_before_any_launch():
     assert lib.tpl_tp_decoder_stack_ex(*args, 7, tpl.BLOCK_SERIAL, None) == unsupported
     assert lib.tpl_tp_decoder_stack_ex(*args, tpl.PATH_AUTO, 5, None) == unsupported
     assert lib.tpl_tp_decoder_stack_path(*args, 9, None) == unsupported
+
+
+def test_vocab_topk_rejects_bad_arguments_before_any_launch():
+    s = ctypes.c_void_p(0)
+    x, w, ws = ctypes.c_void_p(1 << 24), ctypes.c_void_p(2 << 24), ctypes.c_void_p(3 << 24)
+    idx, val = ctypes.c_void_p(4 << 24), ctypes.c_void_p(5 << 24)
+    big = 1 << 30
+
+    def call(*, x=x, w=w, B=4, D=256, V=1000, tp=4, k=2, dtype=tpl.BF16, idx=idx, val=val, sidx=None, sval=None,
+             ws=ws, nbytes=big):
+        return lib.tpl_vocab_parallel_topk(x, w, B, D, V, tp, k, dtype, idx, val, sidx, sval, ws, nbytes, s)
+
+    st, n = _ws(lib.tpl_vocab_parallel_topk_workspace, 4, 1000, 4, 2)
+    assert st == 0 and n > 0
+    assert _ws(lib.tpl_vocab_parallel_topk_workspace, 4, 1000, 3, 2)[0] == 2     # V % tp
+    assert _ws(lib.tpl_vocab_parallel_topk_workspace, 4, 1000, 4, 9)[0] == 2     # k > 8
+    assert _ws(lib.tpl_vocab_parallel_topk_workspace, 4, 16, 4, 5)[0] == 2       # k > V / tp
+    assert _ws(lib.tpl_vocab_parallel_topk_workspace, 0, 1000, 4, 1)[0] == 2     # no tokens
+    assert call(x=None) == 1 and call(idx=None) == 1
+    assert call(D=100) == 2                                   # D % 8
+    assert call(dtype=tpl.F32) == 4
+    assert call(x=ctypes.c_void_p((1 << 24) + 8)) == 3       # X not 16-byte aligned
+    assert call(val=ctypes.c_void_p((5 << 24) + 2)) == 3     # output not 4-byte aligned
+    assert call(nbytes=16) == 5 and call(ws=None) == 5
+    assert call(idx=ctypes.c_void_p((1 << 24) + 64)) == 9    # top_idx inside X
+    assert call(val=ctypes.c_void_p((4 << 24) + 16)) == 9    # top_val overlaps top_idx
+    assert call(sidx=ctypes.c_void_p((3 << 24) + 256)) == 9  # shard output inside the workspace
