@@ -9,11 +9,15 @@
 // tokens (padded to N = 16..128 by the TMA zero fill) the N operand -- so W
 // streams from HBM once per call for B <= 128.  Tiles never straddle a shard:
 // the tile list is shard-major and a shard's last tile masks the rows past its
-// end.  The epilogue ranks each tile's 128 logits per token: each epilogue
-// warp takes its 32 rows by repeated warp max (redux.sync) over an
-// order-preserving integer key, the four warps' lists are merged through
-// shared memory, and the tile's k best candidates per token go to global
-// memory as packed 64-bit words.
+// end.  The epilogue ranks each tile's 128 logits per token: the four
+// epilogue warps turn their TMEM rows into order-preserving integer keys and
+// store them transposed in shared memory (one column per token, padded so both
+// the writes and the column scans are free of bank conflicts); each of the 128
+// threads then scans a slice of one column sequentially, keeping its best k,
+// and one thread per token merges the slices.  The tile's k best candidates
+// per token go to global memory as packed 64-bit words.  No warp-collective
+// rounds are needed, so the ranking stays well inside the time the next tile's
+// weights take to arrive.
 //
 // Kernel 2 (vocab_topk_merge_kernel): one block per (token, shard) reduces
 // that shard's tile candidates to the shard's top-k (the list a device would
@@ -59,12 +63,15 @@ struct VtCfg {
     static constexpr int A_BYTES = VT_BM * VT_BK * 2;               // 16 KB of W
     static constexpr int B_BYTES = BN * VT_BK * 2;                  // tokens
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
     static constexpr int CH = BN >= 32 ? 32 : 16;                    // columns per TMEM load
-    static constexpr int CAND_BYTES = 4 * CH * kVocabTopkMax * 8;   // four warps' lists per column
+    static constexpr int KPAD = VT_BM + 1;                           // padded key column: conflict-free both ways
+    static constexpr int KEY_BYTES = CH * KPAD * 4;                  // one chunk's keys, column-major
+    static constexpr int CAND_BYTES = VT_BM * kVocabTopkMax * 8;     // (row group, column) lists
+    static constexpr int EPI_BYTES = ((KEY_BYTES + 15) & ~15) + CAND_BYTES;
+    static constexpr int STAGES_RAW = (218 * 1024 - EPI_BYTES - 1280) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 10 ? 10 : STAGES_RAW;
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CAND_BYTES + 256 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 256 + 1024;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile must be 16..128 in steps of 16");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -98,6 +105,82 @@ __device__ __forceinline__ bool epi_all(bool p) {
     return r != 0;
 }
 
+// Insert w into the descending list L[0..N), dropping the smallest.
+template <int N>
+__device__ __forceinline__ void list_insert(unsigned long long (&L)[N], unsigned long long w) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const unsigned long long hi = L[i] > w ? L[i] : w;
+        w = L[i] > w ? w : L[i];
+        L[i] = hi;
+    }
+}
+
+// Rank one chunk of CH token columns of a 128-row tile (keys already in
+// s_key, column-major with pitch KPAD).  Thread et scans rows
+// [g CH, (g+1) CH) of column c = et % CH (g = et / CH) and keeps its KL best
+// (KL >= k); after a barrier, thread c < ncols merges the 128 / CH lists of its
+// column and writes the column's k best words to gout[c k ..].  Rows are
+// scanned in ascending order and words compare by (key, lower index), so
+// equal logits resolve to the lower vocabulary index.
+template <int KL, int CH, int KPAD>
+__device__ __forceinline__ void rank_chunk(const uint32_t* s_key, unsigned long long* s_cand, int et, int k,
+                                           uint32_t vtile, unsigned long long* gout, int ncols) {
+    constexpr int G = VT_BM / CH;
+    const int c = et % CH, g = et / CH;
+    const uint32_t* col = s_key + c * KPAD + g * CH;
+    const uint32_t row0 = vtile + (uint32_t)(g * CH);
+    unsigned long long L[KL];
+    if (KL == 1) {
+        uint32_t best = 0u;
+        int at = 0;
+#pragma unroll 8
+        for (int r = 0; r < CH; ++r) {
+            const uint32_t key = col[r];
+            if (key > best) { best = key; at = r; }
+        }
+        L[0] = best ? pack(best, row0 + at) : 0ull;
+    } else {
+#pragma unroll
+        for (int i = 0; i < KL; ++i) L[i] = 0ull;
+#pragma unroll 4
+        for (int r = 0; r < CH; ++r) {
+            const uint32_t key = col[r];
+            if (key) list_insert<KL>(L, pack(key, row0 + r));
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < KL; ++i) s_cand[(g * CH + c) * KL + i] = L[i];
+    epi_sync();
+    if (et < ncols) {                       // et < CH: this thread owns column et (g == 0)
+        if (KL == 1) {
+            unsigned long long best = 0ull;
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                const unsigned long long w = s_cand[gg * CH + c];
+                best = w > best ? w : best;
+            }
+            gout[c] = best;
+        } else {
+            int h[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) h[gg] = 0;
+            for (int i = 0; i < k; ++i) {
+                unsigned long long best = 0ull;
+                int bg = -1;
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    const unsigned long long w = h[gg] < KL ? s_cand[(gg * CH + c) * KL + h[gg]] : 0ull;
+                    if (w > best) { best = w; bg = gg; }
+                }
+                gout[c * k + i] = best;
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) h[gg] += (gg == bg) ? 1 : 0;
+            }
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(VT_THREADS, 1)
 vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -105,8 +188,10 @@ vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     using C = VtCfg<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned long long* s_cand = reinterpret_cast<unsigned long long*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::CAND_BYTES);
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    unsigned long long* s_cand =
+        reinterpret_cast<unsigned long long*>(smem + C::STAGES * C::STAGE_BYTES + ((C::KEY_BYTES + 15) & ~15));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -238,7 +323,7 @@ vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             const int64_t tok0 = (t / p.m_tiles) * BN;
             const int64_t local0 = (int64_t)lt * VT_BM + q * 32;           // shard-local row of lane 0
             const bool row_ok = local0 + lane < p.Vs;
-            const uint32_t vbase = (uint32_t)(s * p.Vs + local0);           // vocabulary index of lane 0
+            const uint32_t vtile = (uint32_t)(s * p.Vs + (int64_t)lt * VT_BM);   // vocabulary index of tile row 0
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             float v[32];
 #pragma unroll 1
@@ -249,48 +334,20 @@ vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&acc_empty[acc]));
                 }
-                // this warp's 32 rows: k rounds of warp max per token column
+                // keys to shared memory, transposed: column j holds the tile's 128 rows
 #pragma unroll
                 for (int j = 0; j < C::CH; ++j) {
                     const bool live = row_ok && tok0 + c0 + j < p.B;
-                    uint32_t key = live ? order_key(v[j]) : 0u;
-                    unsigned long long* dst = s_cand + (q * C::CH + j) * kVocabTopkMax;
-                    for (int i = 0; i < k; ++i) {
-                        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key);
-                        if (m == 0u) {
-                            if (lane == 0) for (int r = i; r < k; ++r) dst[r] = 0ull;
-                            break;
-                        }
-                        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, key == m);
-                        const int l = __ffs(hit) - 1;                // lowest row among equal logits
-                        if (lane == 0) dst[i] = pack(m, vbase + l);
-                        if (lane == l) key = 0u;
-                    }
+                    s_key[j * C::KPAD + q * 32 + lane] = live ? order_key(v[j]) : 0u;
                 }
                 epi_sync();
-                // merge the four sorted lists of one token column per thread
-                if (et < C::CH && tok0 + c0 + et < p.B) {
-                    unsigned long long* out = p.cand + ((int64_t)mg * p.B + tok0 + c0 + et) * k;
-                    const unsigned long long* src = s_cand + et * kVocabTopkMax;
-                    int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
-                    for (int i = 0; i < k; ++i) {
-                        const unsigned long long c0w = h0 < k ? src[(0 * C::CH) * kVocabTopkMax + h0] : 0ull;
-                        const unsigned long long c1w = h1 < k ? src[(1 * C::CH) * kVocabTopkMax + h1] : 0ull;
-                        const unsigned long long c2w = h2 < k ? src[(2 * C::CH) * kVocabTopkMax + h2] : 0ull;
-                        const unsigned long long c3w = h3 < k ? src[(3 * C::CH) * kVocabTopkMax + h3] : 0ull;
-                        const unsigned long long a = c0w > c1w ? c0w : c1w;
-                        const unsigned long long b = c2w > c3w ? c2w : c3w;
-                        const unsigned long long best = a > b ? a : b;
-                        out[i] = best;
-                        if (best != 0ull) {
-                            if (best == c0w) ++h0;
-                            else if (best == c1w) ++h1;
-                            else if (best == c2w) ++h2;
-                            else ++h3;
-                        }
-                    }
-                }
-                epi_sync();
+                const int64_t left = p.B - (tok0 + c0);
+                const int ncols = left < C::CH ? (int)left : C::CH;
+                unsigned long long* gout = p.cand + ((int64_t)mg * p.B + tok0 + c0) * k;
+                if (k == 1) rank_chunk<1, C::CH, C::KPAD>(s_key, s_cand, et, k, vtile, gout, ncols);
+                else if (k == 2) rank_chunk<2, C::CH, C::KPAD>(s_key, s_cand, et, k, vtile, gout, ncols);
+                else if (k <= 4) rank_chunk<4, C::CH, C::KPAD>(s_key, s_cand, et, k, vtile, gout, ncols);
+                else rank_chunk<8, C::CH, C::KPAD>(s_key, s_cand, et, k, vtile, gout, ncols);
             }
         }
     }
@@ -301,16 +358,6 @@ vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
-    }
-}
-
-// Insert w into the descending list L[0..kVocabTopkMax), dropping the smallest.
-__device__ __forceinline__ void list_insert(unsigned long long (&L)[kVocabTopkMax], unsigned long long w) {
-#pragma unroll
-    for (int i = 0; i < kVocabTopkMax; ++i) {
-        const unsigned long long hi = L[i] > w ? L[i] : w;
-        w = L[i] > w ? w : L[i];
-        L[i] = hi;
     }
 }
 
@@ -362,7 +409,7 @@ vocab_topk_merge_kernel(const unsigned long long* __restrict__ cand, unsigned lo
     const int n = tiles_per_shard * k;
     for (int c = threadIdx.x; c < n; c += VT_MERGE_THREADS) {
         const int lt = c / k, i = c - lt * k;
-        list_insert(L, cand[(((int64_t)s * tiles_per_shard + lt) * B + b) * k + i]);
+        list_insert<kVocabTopkMax>(L, cand[(((int64_t)s * tiles_per_shard + lt) * B + b) * k + i]);
     }
     block_topk(L, k, s_out, s_red);
     if (threadIdx.x < k) {
@@ -388,7 +435,7 @@ vocab_topk_merge_kernel(const unsigned long long* __restrict__ cand, unsigned lo
     for (int i = 0; i < kVocabTopkMax; ++i) L[i] = 0ull;
     for (int c = threadIdx.x; c < tp * k; c += VT_MERGE_THREADS) {
         const int ss = c / k, i = c - ss * k;
-        list_insert(L, __ldcg(shard_best + ((int64_t)ss * B + b) * k + i));
+        list_insert<kVocabTopkMax>(L, __ldcg(shard_best + ((int64_t)ss * B + b) * k + i));
     }
     block_topk(L, k, s_out, s_red);
     if (threadIdx.x < k) {
