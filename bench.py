@@ -63,9 +63,11 @@ def args_parse():
     ap.add_argument("--no-llama", action="store_true", help="skip the Llama-3.1-70B-shaped decode stack")
     ap.add_argument("--no-cases", action="store_true", help="skip the sharded-matmul cases and shard_reduce")
     ap.add_argument("--no-lm-head", action="store_true", help="skip the vocabulary-parallel lm_head lines")
-    ap.add_argument("--lm-head-model", choices=["llama-3.1-70b", "qwen2.5-1.5b"], default=None,
-                    help="with --only lm_head: one model's shape only (--batches selects the batch sizes)")
-    ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head"], default=None,
+    ap.add_argument("--no-w8", action="store_true", help="skip the weight-only int8 MLP lines")
+    ap.add_argument("--model", "--lm-head-model", dest="model", choices=["llama-3.1-70b", "qwen2.5-1.5b"],
+                    default=None, help="with --only lm_head or --only w8: one model's shape only "
+                                       "(--batches selects the batch sizes)")
+    ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head", "w8"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
     ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
@@ -510,7 +512,7 @@ def run_lm_head(args, tpl, dev, peaks, stream, k=1):
     out = {}
     reps = max(5, args.steps // 2)
     for name, c in LM_HEADS.items():
-        if args.only == "lm_head" and args.lm_head_model not in (None, name):
+        if args.only == "lm_head" and args.model not in (None, name):
             continue
         D, V, tp = c["D"], c["V"], c["tp"]
         batches = c["batches"]
@@ -546,6 +548,83 @@ def run_lm_head(args, tpl, dev, peaks, stream, k=1):
             del g
         out[name] = res
         del x_all, W
+        torch.cuda.empty_cache()
+    return out
+
+
+# Weight-only int8 decode MLP shapes (the decode configurations' MLPs).
+W8_MLPS = {
+    "qwen2.5-1.5b": {"D": 1536, "F": 8960, "tp": 2, "batches": (1, 8, 32, 64)},
+    "llama-3.1-70b": {"D": 8192, "F": 28672, "tp": 8, "batches": (1, 8, 32, 64)},
+}
+L2_BYTES = 126 * 2 ** 20
+
+
+def run_w8_mlp(args, tpl, dev, peaks, stream):
+    """Decode MLP with int8 weights against the same MLP in bf16.  Enough
+    distinct weight copies are cycled that every timed pass streams more than
+    three L2s of int8 weights; GB/s counts the bytes each MLP must read
+    (int8 codes + float32 scales, or bf16 weights) per forward."""
+    out = {}
+    reps = max(3, args.steps // 5)
+    for name, c in W8_MLPS.items():
+        if args.only == "w8" and args.model not in (None, name):
+            continue
+        D, F, tp = c["D"], c["F"], c["tp"]
+        batches = c["batches"]
+        if args.only == "w8" and args.batches:
+            batches = tuple(int(b) for b in args.batches.split(","))
+        b8 = 3 * D * F + 4 * (2 * F + D * tp)
+        b16 = 3 * D * F * 2
+        copies = max(1, math.ceil(3 * L2_BYTES / b8))
+        weights = []
+        for i in range(copies):
+            Wg = si.normal((F, D), 0.02, 0, f"{name}.w8.Wg{i}", device=dev)
+            Wu = si.normal((F, D), 0.02, 0, f"{name}.w8.Wu{i}", device=dev)
+            Wd = si.normal((D, F), 0.02, 0, f"{name}.w8.Wd{i}", device=dev)
+            q = tpl.quantize_w8(Wg) + tpl.quantize_w8(Wu) + tpl.quantize_w8(Wd, groups=tp)
+            weights.append(((Wg, Wu, Wd), q))
+        res = {"workload": f"{name}-shaped decode MLP D={D} F={F}, TP={tp}: int8 weights "
+                           f"({b8 / 1e6:.1f} MB) vs bf16 ({b16 / 1e6:.1f} MB), {copies} weight copies cycled",
+               "per_batch": {}}
+        for B in batches:
+            x = si.activations(B, D, seed=5, name=f"{name}.w8.x{B}", device=dev)
+            y8 = torch.empty(B, D, dtype=torch.bfloat16, device=dev)
+            y16 = torch.empty_like(y8)
+            ws8 = tpl.workspace(tpl.mlp_w8_workspace_bytes(B, D, F, tp), dev)
+            ws16 = torch.empty(tpl.mlp_workspace_bytes(B, D, F, tp), dtype=torch.uint8, device=dev)
+            times = {}
+            for kind in ("w8", "bf16"):
+                def call():
+                    for (Wg, Wu, Wd), q in weights:
+                        if kind == "w8":
+                            tpl.tp_mlp_forward_w8(x, *q, tp, out=y8, ws=ws8)
+                        else:
+                            tpl.tp_mlp_forward(x, Wg, Wu, Wd, tp, out=y16, ws=ws16)
+                with torch.cuda.stream(stream):
+                    call()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    call()
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(reps):
+                    g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                times[kind] = a.elapsed_time(b) / reps / copies
+                del g
+            gbs = b8 / (times["w8"] / 1e3) / 1e9
+            res["per_batch"][str(B)] = {"ms_int8": times["w8"], "ms_bf16": times["bf16"],
+                                        "speedup": times["bf16"] / times["w8"], "int8_GB/s": gbs,
+                                        "frac_of_peak": gbs / peaks["hbm_gbs"],
+                                        "bf16_GB/s": b16 / (times["bf16"] / 1e3) / 1e9}
+        out[name] = res
+        del weights
         torch.cuda.empty_cache()
     return out
 
@@ -653,6 +732,11 @@ def main():
             print(json.dumps(dict(pre, metric=METRIC, n_gpus=world, steps=args.steps, warmup=args.warmup)),
                   flush=True)
         return
+    if args.only == "w8":
+        w8 = run_w8_mlp(args, tpl, dev, peaks, stream)
+        if rank == 0:
+            print(json.dumps(dict(w8_mlp=w8, metric=METRIC, n_gpus=world, steps=args.steps)), flush=True)
+        return
     if args.only == "lm_head":
         lm = run_lm_head(args, tpl, dev, peaks, stream)
         if rank == 0:
@@ -679,6 +763,10 @@ def main():
     if not args.no_lm_head and args.only is None:
         lm_head = run_lm_head(args, tpl, dev, peaks, stream)
 
+    w8 = None
+    if not args.no_w8 and args.only is None:
+        w8 = run_w8_mlp(args, tpl, dev, peaks, stream)
+
     cases = reduce_line = None
     if not args.no_cases and args.only is None:
         cases, reduce_line = run_cases_and_reduce(args, tpl, dev, peaks, peak_kind)
@@ -702,7 +790,7 @@ def main():
                 "gpu_launches": dec["gpu_launches"], "clocks": dec["clocks"],
                 "per_batch": dec["per_batch"], "kernel_share": dec["kernel_share"],
                 "qwen_decode_parallel_block": parallel, "llama_decode": llama,
-                "prefill": prefill, "lm_head_topk": lm_head, "sharded_matmul": cases,
+                "prefill": prefill, "lm_head_topk": lm_head, "mlp_int8_weights": w8, "sharded_matmul": cases,
                 "shard_reduce": reduce_line}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -279,6 +279,46 @@ tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void* const* Wq
                                    void* stream);
 
 /* --------------------------------------------------------------------------
+ * Weight-only int8 decode MLP ("Lecture 4 - Distributed Serving", S5.5: only
+ * the weights are quantised, which cuts the time spent reading them; S6.2: the
+ * cheapest configurations are those whose weights take half the bytes).
+ *
+ * tpl_quantize_w8: symmetric per-(row, column group) quantisation of a bf16
+ * matrix W [rows, cols] (row-major, read only).  Row r is split into `groups`
+ * contiguous groups of cols/groups columns; group g gets
+ * scale[r * groups + g] = amax(|W[r, group g]|) / 127 (float32) and
+ * Q[r, c] = clamp(round_half_even(W[r, c] / scale), -127, 127) (int8,
+ * row-major), the division in IEEE float32; a group of zeros gets scale 0 and
+ * codes 0.  Use groups = 1 for Wg and Wu ([F, D]) and groups = tp for Wd
+ * ([D, F], row-parallel), so that every shard's codes depend only on the
+ * weights that shard holds.  Requires (cols / groups) % 8 == 0 and W 16-byte,
+ * Q 8-byte, scale 4-byte aligned (TPL_ERR_ALIGN), no overlap (TPL_ERR_ALIAS).
+ *
+ * tpl_tp_mlp_forward_w8: tp_mlp_forward with int8 weights and bf16
+ * activations.  Computes exactly what tp_mlp_forward computes on the
+ * dequantised weights Q * scale: H = bf16(silu(X Wg^T) * (X Wu^T)), per-shard
+ * fp32 partials of H Wd^T, summed in ascending shard order into Y.
+ *   X [B, D] bf16; Qg, Qu [F, D] int8 with sg, su [F]; Qd [D, F] int8 with
+ *   sd [D, tp]; Y [B, D] of out_dtype (TPL_BF16 or TPL_F32); partials
+ *   (optional) [tp, B, D] fp32.  Requires F % tp == 0, D % 64 == 0,
+ *   (F / tp) % 64 == 0 (TPL_ERR_SHAPE); X, Y, partials, Q* and ws 16-byte
+ *   aligned, scales 4-byte aligned (TPL_ERR_ALIGN); ws of at least
+ *   tpl_tp_mlp_forward_w8_workspace bytes (TPL_ERR_WORKSPACE; nothing in it
+ *   needs to start at zero); outputs and ws disjoint from the inputs
+ *   (TPL_ERR_ALIAS); the sm_103 tensor-core path (TPL_ERR_UNSUPPORTED).
+ *   The int8 tiles are widened to bf16 on the chip and multiplied on the
+ *   tensor cores; every int8 value is a bf16 value, so only the accumulation
+ *   order differs from the bf16 call.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_quantize_w8(const void* W, int64_t rows, int64_t cols, int groups, int8_t* Q,
+                           float* scale, void* stream);
+tpl_status tpl_tp_mlp_forward_w8_workspace(int64_t B, int64_t D, int64_t F, int tp, size_t* bytes);
+tpl_status tpl_tp_mlp_forward_w8(const void* X, const int8_t* Qg, const float* sg, const int8_t* Qu,
+                                 const float* su, const int8_t* Qd, const float* sd, void* Y,
+                                 float* partials, int64_t B, int64_t D, int64_t F, int tp,
+                                 int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * Vocabulary-parallel lm_head with a top-k candidate exchange
  * ("Lecture 4 - Distributed Serving", S4.5 "lm_head and sequence parallelism").
  * The lm_head is split by vocabulary: shard s owns the rows

@@ -62,6 +62,10 @@ _SIGS = {
     "tpl_tp_decoder_stack": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                     ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
                                     _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tpl_quantize_w8": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "tpl_tp_mlp_forward_w8_workspace": (_i32, [_i64, _i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "tpl_tp_mlp_forward_w8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32,
+                                     _vp, _sz, _vp]),
     "tpl_vocab_parallel_topk_workspace": (_i32, [_i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
     "tpl_vocab_parallel_topk": (_i32, [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                        _sz, _vp]),
@@ -411,3 +415,43 @@ def vocab_parallel_topk(x, W, tp: int, k: int = 1, shard_outputs: bool = False, 
                                        _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "tpl_vocab_parallel_topk")
     return (idx, val, sidx, sval) if shard_outputs else (idx, val)
+
+
+def quantize_w8(W, groups: int = 1, stream=None):
+    """Symmetric int8 codes of a bf16 matrix W [rows, cols], one float32 scale
+    per row and column group: returns (Q int8 [rows, cols], scale [rows, groups])."""
+    _contig(W)
+    rows, cols = W.shape
+    Q = torch.empty(rows, cols, dtype=torch.int8, device=W.device)
+    scale = torch.empty(rows, groups, dtype=torch.float32, device=W.device)
+    _check(lib.tpl_quantize_w8(_p(W), rows, cols, groups, _p(Q), _p(scale), _stream(stream)), "tpl_quantize_w8")
+    return Q, scale
+
+
+def mlp_w8_workspace_bytes(B, D, F, tp) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.tpl_tp_mlp_forward_w8_workspace(B, D, F, tp, ctypes.byref(n)), "tpl_tp_mlp_forward_w8_workspace")
+    return n.value
+
+
+def tp_mlp_forward_w8(X, Qg, sg, Qu, su, Qd, sd, tp: int, out=None, partials=None, out_dtype=None, ws=None,
+                      stream=None):
+    """tp_mlp_forward with int8 weights (codes and scales from quantize_w8:
+    groups 1 for Qg/Qu [F, D], groups tp for Qd [D, F]); X is bf16."""
+    _contig(X, Qg, sg, Qu, su, Qd, sd)
+    B, D = X.shape
+    F = Qg.shape[0]
+    odt = _out_code(BF16, out, out_dtype)
+    if out is None:
+        out = torch.empty(B, D, dtype=_tdt(odt), device=X.device)
+    want_p = partials is True or isinstance(partials, torch.Tensor)
+    if partials is True:
+        partials = torch.empty(tp, B, D, dtype=torch.float32, device=X.device)
+    elif not want_p:
+        partials = None
+    nbytes = mlp_w8_workspace_bytes(B, D, F, tp)
+    ws = workspace(nbytes, X.device) if ws is None else ws
+    _check(lib.tpl_tp_mlp_forward_w8(_p(X), _p(Qg), _p(sg), _p(Qu), _p(su), _p(Qd), _p(sd), _p(out), _p(partials),
+                                     B, D, F, tp, odt, _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpl_tp_mlp_forward_w8")
+    return (out, partials) if want_p else out

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtpl.so")
-SOURCES = ["api.cu", "simt.cu", "tc_gemm.cu", "decode_fused.cu", "static_ws.cu", "vocab_topk.cu"]
+SOURCES = ["api.cu", "simt.cu", "tc_gemm.cu", "decode_fused.cu", "static_ws.cu", "vocab_topk.cu", "w8_gemm.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))] + \
           [os.path.join(ROOT, "include", "tpl.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

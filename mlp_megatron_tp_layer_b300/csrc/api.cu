@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "w8.h"
 
 namespace tpl {
 
@@ -753,6 +754,126 @@ extern "C" tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* W
     const void* u[1] = {Wu};
     const void* d[1] = {Wd};
     return tpl_tp_decoder_stack(x, y, q, o, g, u, d, 1, B, D, F, n_q, n_kv, head_dim, tp, ws, ws_bytes, stream);
+}
+
+// ------------------------------------------------- weight-only int8 MLP
+
+namespace {
+struct W8Plan {
+    KSplit ks_gu;   // gate/up: K = D, one shard, split into chunks to fill the machine
+    KSplit ks_d;    // down: K = F, tp shards, each split into chunks
+    size_t h_off, gu_off, gu2_off, part_off, total;
+};
+W8Plan plan_mlp_w8(int64_t B, int64_t D, int64_t F, int tp) {
+    W8Plan p{};
+    const int64_t ntok = (B + 127) / 128;
+    p.ks_gu = choose_split((F + 127) / 128 * ntok, D, 1, 256, 64);
+    p.ks_d = choose_split((D + 127) / 128 * ntok, F / tp, tp, 256, 64);
+    p.h_off = 0;
+    p.gu_off = up((size_t)B * F * 2);
+    const size_t gu = p.ks_gu.sub > 1 ? up((size_t)p.ks_gu.sub * B * F * 4) : 0;
+    p.gu2_off = p.gu_off + gu;
+    p.part_off = p.gu2_off + gu;
+    p.total = p.part_off + up((size_t)p.ks_d.tp * p.ks_d.sub * B * D * 4);
+    return p;
+}
+tpl_status check_w8_shape(int64_t B, int64_t D, int64_t F, int tp) {
+    if (B <= 0 || D <= 0 || F <= 0 || tp <= 0 || F % tp != 0) return TPL_ERR_SHAPE;
+    if (D % 64 != 0 || (F / tp) % 64 != 0) return TPL_ERR_SHAPE;
+    return TPL_OK;
+}
+bool al8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+}  // namespace
+
+extern "C" tpl_status tpl_quantize_w8(const void* W, int64_t rows, int64_t cols, int groups, int8_t* Q,
+                                      float* scale, void* stream) {
+    if (!W || !Q || !scale) return TPL_ERR_NULL;
+    if (rows <= 0 || cols <= 0 || groups <= 0 || cols % groups != 0) return TPL_ERR_SHAPE;
+    if ((cols / groups) % 8 != 0) return TPL_ERR_ALIGN;
+    if (!al16(W) || !al8(Q) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0) return TPL_ERR_ALIGN;
+    const size_t wb = (size_t)rows * cols * 2, qb = (size_t)rows * cols, sb = (size_t)rows * groups * 4;
+    if (overlap(Q, qb, W, wb) || overlap(scale, sb, W, wb) || overlap(scale, sb, Q, qb)) return TPL_ERR_ALIAS;
+    if (!device_ctx()) return TPL_ERR_CUDA;
+    cudaStream_t st = S(stream);
+    ProfScope prof("quantize_w8", st);
+    return cuda_status(launch_quantize_w8(W, rows, cols, groups, Q, scale, st));
+}
+
+extern "C" tpl_status tpl_tp_mlp_forward_w8_workspace(int64_t B, int64_t D, int64_t F, int tp, size_t* bytes) {
+    if (!bytes) return TPL_ERR_NULL;
+    const tpl_status s = check_w8_shape(B, D, F, tp);
+    if (s != TPL_OK) return s;
+    *bytes = plan_mlp_w8(B, D, F, tp).total;
+    return TPL_OK;
+}
+
+extern "C" tpl_status tpl_tp_mlp_forward_w8(const void* X, const int8_t* Qg, const float* sg, const int8_t* Qu,
+                                            const float* su, const int8_t* Qd, const float* sd, void* Y,
+                                            float* partials, int64_t B, int64_t D, int64_t F, int tp,
+                                            int out_dtype, void* ws, size_t ws_bytes, void* stream) {
+    if (!X || !Qg || !sg || !Qu || !su || !Qd || !sd || !Y) return TPL_ERR_NULL;
+    tpl_status s = check_w8_shape(B, D, F, tp);
+    if (s != TPL_OK) return s;
+    if (out_dtype != TPL_F32 && out_dtype != TPL_BF16) return TPL_ERR_DTYPE;
+    if (!al16(X) || !al16(Qg) || !al16(Qu) || !al16(Qd) || !al16(Y) || (partials && !al16(partials)) ||
+        (ws && !al16(ws)))
+        return TPL_ERR_ALIGN;
+    const void* f4[3] = {sg, su, sd};
+    for (const void* q : f4)
+        if ((reinterpret_cast<uintptr_t>(q) & 3u) != 0) return TPL_ERR_ALIGN;
+    const W8Plan p = plan_mlp_w8(B, D, F, tp);
+    if (!ws || ws_bytes < p.total) return TPL_ERR_WORKSPACE;
+    const size_t ybytes = (size_t)B * D * esize(out_dtype), wq = (size_t)F * D, xb = (size_t)B * D * 2;
+    const size_t pb = (size_t)tp * B * D * 4;
+    const void* ins[7] = {X, Qg, Qu, Qd, sg, su, sd};
+    const size_t insz[7] = {xb, wq, wq, wq, (size_t)F * 4, (size_t)F * 4, (size_t)D * tp * 4};
+    for (int i = 0; i < 7; ++i) {
+        if (overlap(Y, ybytes, ins[i], insz[i]) || overlap(ws, p.total, ins[i], insz[i])) return TPL_ERR_ALIAS;
+        if (partials && overlap(partials, pb, ins[i], insz[i])) return TPL_ERR_ALIAS;
+    }
+    if (overlap(Y, ybytes, ws, p.total) || (partials && (overlap(partials, pb, ws, p.total) ||
+                                                         overlap(partials, pb, Y, ybytes))))
+        return TPL_ERR_ALIAS;
+    if (!device_ctx()) return TPL_ERR_CUDA;
+    if (!tc_gemm_supported()) return TPL_ERR_UNSUPPORTED;
+    cudaStream_t st = S(stream);
+    char* w = static_cast<char*>(ws);
+    void* H = w + p.h_off;
+
+    W8GemmArgs g{};
+    g.Q = Qg; g.Q2 = Qu; g.scale = sg; g.scale2 = su; g.groups = 1;
+    g.M = F; g.X = X; g.ldx = D; g.N = B; g.K = D; g.ks = p.ks_gu;
+    float* gp = reinterpret_cast<float*>(w + p.gu_off);
+    float* up_p = reinterpret_cast<float*>(w + p.gu2_off);
+    if (p.ks_gu.sub == 1) {
+        g.epi.mode = EPI_SWIGLU; g.epi.out = H; g.epi.out_bf16 = 1; g.epi.ldo = F;
+    } else {
+        g.epi.mode = EPI_PARTIAL2; g.epi.out32 = gp; g.epi.out32b = up_p; g.epi.ldo = F;
+        g.epi.split_stride = B * F;
+    }
+    {
+        ProfScope prof("w8_gateup", st);
+        if (launch_w8_gemm(g, st) != cudaSuccess) return TPL_ERR_CUDA;
+    }
+    if (p.ks_gu.sub > 1) {
+        // SwiGLU of the chunk sums (chunks added in K order), stored bf16
+        ReduceArgs r{};
+        r.ws = gp; r.ws_up = up_p; r.rows = B; r.cols = F; r.tp = 1; r.sub = p.ks_gu.sub;
+        r.y = H; r.y_bf16 = 1; r.mode = TPL_ALLREDUCE; r.eps = kRmsEpsilon;
+        ProfScope prof("reduce", st);
+        if (launch_reduce(r, st) != cudaSuccess) return TPL_ERR_CUDA;
+    }
+    W8GemmArgs d{};
+    d.Q = Qd; d.scale = sd; d.groups = tp;
+    d.M = D; d.X = H; d.ldx = F; d.N = B; d.K = F; d.ks = p.ks_d;
+    float* part = reinterpret_cast<float*>(w + p.part_off);
+    d.epi = epi_partial(part, D, B * D);
+    {
+        ProfScope prof("w8_down", st);
+        if (launch_w8_gemm(d, st) != cudaSuccess) return TPL_ERR_CUDA;
+    }
+    return cuda_status(reduce_into(part, B, D, p.ks_d, partials, Y, out_dtype == TPL_BF16, TPL_ALLREDUCE, nullptr,
+                                   nullptr, nullptr, st));
 }
 
 // ----------------------------------------------- vocabulary-parallel lm_head
