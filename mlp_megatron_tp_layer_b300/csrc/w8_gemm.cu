@@ -4,25 +4,29 @@
 //
 // Q streams from HBM as int8, half the bytes of bf16 ("Lecture 4 - Distributed
 // Serving", S5.5: only the weights are quantised, to cut the time spent
-// reading them).  tcgen05.mma has no int8 x bf16 form, so eight converter warps
-// widen each 128 x 64 int8 tile to bf16 -- exactly: every integer in
-// [-127, 127] is a bf16 value -- straight into the 128B-swizzled K-major layout
-// that the MMA's shared-memory descriptor expects, and the per-row scale
-// multiplies the fp32 accumulator in the epilogue.
+// reading them).  tcgen05.mma has no int8 x bf16 form, so converter warps
+// widen the weights to bf16 -- exactly: every integer in [-127, 127] is a bf16
+// value -- and store them into tensor memory, where the MMA reads its A
+// operand (weights are the M = 128 side, one row per TMEM lane); the tokens
+// stay in shared memory as the B operand, and the per-row scale multiplies the
+// fp32 accumulator in the epilogue.  Shared memory then carries only the TMA
+// writes and one read of each int8 byte; a widened copy in shared memory
+// would cost three times the int8 bytes again and makes shared-memory
+// bandwidth, not HBM, the limit.
 //
-// Rings: the TMA ring carries the int8 weight tile(s) and the bf16 token tiles
-// of one 128-wide K block per stage -- 128 bytes of each weight row, the same
-// bytes per row as a bf16 tile, so the copy engine moves as many bytes per
-// request as on the bf16 path -- and holds the bytes in flight from HBM; the
-// converted ring holds widened 64-wide K halves (two or three stages).  A TMA
-// stage is released by the commit of the MMAs that read its token tiles, which
+// Rings: the TMA ring (shared memory) carries the int8 weight tile(s) and the
+// bf16 token tiles of one 128-wide K block per stage -- 128 bytes of each
+// weight row, so every copy request moves as many bytes as on the bf16 path.
+// The operand ring (TMEM columns) holds widened 64-wide K halves.  A TMA stage
+// is released by the commit of the MMAs that read its token tiles, which
 // come after the converters have read its weights.
 //
 // Warp roles (448 threads): 0 TMA producer; 1 TMEM owner + MMA issuer;
-// 2-5 epilogue (TMEM lanes 32*(w%4)); 6-13 converters (half a weight row each,
-// two warps per SM sub-partition so one's latency hides behind the other).
-// Every wait is bounded; on expiry the CTA sets the sticky device error word,
-// drains what it started, frees TMEM and exits.
+// 2-5 epilogue; 6-13 converters.  A warp reaches only the TMEM lanes
+// 32*(w%4)..+31, so epilogue warp w reads and converter warp w writes the rows
+// of that lane quarter; converter warps 6-9 take the first 32 K elements of a
+// half, 10-13 the second.  Every wait is bounded; on expiry the CTA sets the
+// sticky device error word, drains what it started, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -40,10 +44,11 @@ namespace tpl {
 namespace {
 
 constexpr int W8_BM = 128;          // weight rows per tile (TMEM lanes)
-constexpr int W8_BK = 64;           // K elements per widened tile (one MMA group)
+constexpr int W8_BK = 64;           // K elements per widened operand stage (one MMA group)
 constexpr int W8_RK = 128;          // K elements per TMA stage (128 int8 bytes per row)
 constexpr int W8_THREADS = 448;
 constexpr int W8_CONV_WARPS = 8;
+constexpr int W8_TMEM_COLS = 512;   // the whole TMEM of the SM (one CTA per SM)
 
 struct W8Params {
     int64_t M, NB;
@@ -64,19 +69,19 @@ struct W8Cfg {
     static constexpr int X_HALF = BN * W8_BK * 2;                 // token tile of one 64-wide K half
     static constexpr int X_BYTES = 2 * X_HALF;                    // token tiles first in the stage
     static constexpr int RAW_BYTES = X_BYTES + NA * Q_BYTES;
-    static constexpr int CONV_TILE = W8_BM * W8_BK * 2;           // 16 KB widened tile
-    static constexpr int CONV_BYTES = NA * CONV_TILE;
-    static constexpr int CSTAGES = DUAL ? 2 : 3;
-    static constexpr int STAGES_RAW = (200 * 1024 - CSTAGES * CONV_BYTES) / RAW_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
+    static constexpr int STAGES_RAW = (200 * 1024) / RAW_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    // TMEM: accumulators (two if they fit beside four operand stages), then operand stages
     static constexpr int ACC_COLS = DUAL ? 2 * BN : BN;
-    static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32) ? 32 : (2 * ACC_COLS <= 64) ? 64
-                                   : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
-    static constexpr int SMEM_BYTES = CSTAGES * CONV_BYTES + STAGES * RAW_BYTES + 512 + 1024;
+    static constexpr int A_COLS = NA * (W8_BK / 2);               // 64 bf16 = 32 columns per operand
+    static constexpr int NACC = (2 * ACC_COLS + 4 * A_COLS <= W8_TMEM_COLS) ? 2 : 1;
+    static constexpr int A_BASE = NACC * ACC_COLS;
+    static constexpr int CSTAGES_RAW = (W8_TMEM_COLS - A_BASE) / A_COLS;
+    static constexpr int CSTAGES = CSTAGES_RAW > 4 ? 4 : CSTAGES_RAW;
+    static constexpr int SMEM_BYTES = STAGES * RAW_BYTES + 512 + 1024;
     static_assert(RAW_BYTES % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
-    static_assert(STAGES >= 2, "TMA ring depth");
+    static_assert(STAGES >= 2 && CSTAGES >= 2, "ring depths");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(2 * ACC_COLS <= 512, "TMEM holds 512 fp32 columns");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile 16..128 in steps of 16");
 };
 
@@ -97,21 +102,40 @@ __device__ __forceinline__ void split_range(const W8Params& p, int sp, int64_t& 
     nkb = (int)((k1 - k0 + W8_BK - 1) / W8_BK);
 }
 
-// Widen 32 int8 weights of row r into that row of a 128B-swizzled bf16 tile
-// (64 K elements): K half hh of the 128-wide int8 row (itself 128B-swizzled by
-// the copy), quarter h of that half.  16-byte chunk c of a row lives at chunk
-// position c ^ (r % 8) in both tiles.  An int8 q becomes the float
-// 2^23 + (q + 128) by placing its biased byte under the exponent bits of 2^23;
-// subtracting 2^23 + 128 leaves q exactly, and since |q| <= 128 has at most
-// eight significant bits its bf16 value is the float's upper half.
-__device__ __forceinline__ void widen(const uint8_t* q_row, uint8_t* dst_row, int r, int hh, int h) {
+// tcgen05.mma with the A operand in tensor memory (kind::f16, bf16 x bf16 -> fp32).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp writes lane base+i.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Widen 32 int8 weights of row r -- K elements 64 hh + 32 kq .. +31 of the
+// 128-wide int8 row, itself 128B-swizzled by the copy (16-byte chunk c at
+// position c ^ (r % 8)) -- into 16 words of bf16 pairs, lower K in the low
+// half.  An int8 q becomes the float 2^23 + (q + 128) by placing its biased
+// byte under the exponent bits of 2^23; subtracting 2^23 + 128 leaves q
+// exactly, and since |q| <= 128 has at most eight significant bits its bf16
+// value is the float's upper half.
+__device__ __forceinline__ void widen(const uint8_t* q_row, int r, int hh, int kq, uint32_t (&out)[16]) {
     const int sw = r & 7;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const int ci = 4 * hh + 2 * h + j;                      // int8 chunk: 16 K elements
+        const int ci = 4 * hh + 2 * kq + j;                     // int8 chunk: 16 K elements
         const uint4 w = *reinterpret_cast<const uint4*>(q_row + ((ci ^ sw) << 4));
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-        uint32_t out[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t b = words[i] ^ 0x80808080u;
@@ -119,12 +143,9 @@ __device__ __forceinline__ void widen(const uint8_t* q_row, uint8_t* dst_row, in
             const float f1 = __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7541)) - 8388736.0f;
             const float f2 = __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7542)) - 8388736.0f;
             const float f3 = __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7543)) - 8388736.0f;
-            out[2 * i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-            out[2 * i + 1] = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+            out[8 * j + 2 * i] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+            out[8 * j + 2 * i + 1] = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
         }
-        const int cb = 4 * h + 2 * j;                           // bf16 chunks cb, cb + 1: 8 K elements each
-        *reinterpret_cast<uint4*>(dst_row + ((cb ^ sw) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(dst_row + (((cb + 1) ^ sw) << 4)) = make_uint4(out[4], out[5], out[6], out[7]);
     }
 }
 
@@ -134,9 +155,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmX, const W8Params p) {
     using C = W8Cfg<BN, DUAL>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* conv = smem;                                   // [CSTAGES][NA] widened 16 KB tiles
-    uint8_t* raw = smem + C::CSTAGES * C::CONV_BYTES;       // [STAGES] token tile | int8 tile(s)
+    uint8_t* raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + C::STAGES * C::RAW_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
@@ -171,7 +190,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         prefetch_tmap(&tmX);
         if (DUAL) prefetch_tmap(&tmQ2);
     }
-    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), W8_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -238,28 +257,28 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 int64_t k0;
                 int nkb;
                 split_range(p, c.sp, k0, nkb);
-                const int acc = it & 1;
-                const uint32_t acc_phase = (it >> 1) & 1;
+                const int acc = it % C::NACC;
+                const uint32_t acc_phase = (it / C::NACC) & 1;
                 if (!mbar_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * C::ACC_COLS;
                 for (int kb = 0; kb < nkb && ok; kb += 2) {
                     const int halves = min(2, nkb - kb);
                     for (int hh = 0; hh < halves; ++hh) {
-                        // widened weights ready (the converters saw the stage land);
+                        // widened weights in TMEM (the converters saw the stage land);
                         // the token tiles' own barrier is already complete by then
                         if (!mbar_wait(smem_addr(&cfull[cst]), cph, abort_flag) ||
                             !mbar_wait(smem_addr(&full[stage]), phase, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t sa = smem_addr(conv + cst * C::CONV_BYTES);
+                        const uint32_t a = tmem_base + C::A_BASE + cst * C::A_COLS;
                         const uint32_t sb = smem_addr(raw + stage * C::RAW_BYTES + hh * C::X_HALF);
 #pragma unroll
                         for (int kk = 0; kk < W8_BK / 16; ++kk) {
                             const uint32_t accum = (kb | hh | kk) ? 1u : 0u;
-                            mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc, accum);
-                            if (DUAL)
-                                mma_bf16(d + BN, sw128_desc(sa + C::CONV_TILE + kk * 32), sw128_desc(sb + kk * 32),
-                                         idesc, accum);
+                            // K = 16 bf16 per instruction: 8 TMEM columns of A, 32 bytes of the B row
+                            mma_bf16_ta(d, a + kk * 8, sw128_desc(sb + kk * 32), idesc, accum);
+                            if (DUAL) mma_bf16_ta(d + BN, a + W8_BK / 2 + kk * 8, sw128_desc(sb + kk * 32), idesc,
+                                                  accum);
                         }
                         mma_commit(smem_addr(&cempty[cst]));
                         if (++cst == C::CSTAGES) { cst = 0; cph ^= 1; }
@@ -283,8 +302,8 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         int it = 0;
         for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
             const TileCoord c = tile_coord(p, t);
-            const int acc = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
+            const int acc = it % C::NACC;
+            const uint32_t acc_phase = (it / C::NACC) & 1;
             const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&acc_full[acc]), acc_phase, abort_flag));
             if (!ok) { if (lane == 0) fail(); break; }
             tc_fence_after();
@@ -319,8 +338,10 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
     } else {
         // ---------------------------------------------------------- converters
-        const int ct = threadIdx.x - 192;       // 0..255
-        const int r = ct >> 1, h = ct & 1;      // weight row within the tile, quarter of the 128-wide row
+        const int q = warp & 3;                 // TMEM lane quarter this warp may write
+        const int kq = (warp - 6) >> 2;         // which 32 of a half's 64 K elements
+        const int r = q * 32 + lane;            // weight row within the tile = TMEM lane
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + C::A_BASE + kq * 16;
         int stage = 0, cst = 0;
         uint32_t phase = 0, cph = 0;
         bool ok = true;
@@ -337,15 +358,19 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 const uint8_t* src = raw + stage * C::RAW_BYTES + C::X_BYTES + r * W8_RK;
                 for (int hh = 0; hh < halves; ++hh) {
+                    uint32_t wa[16], wb[16];
+                    widen(src, r, hh, kq, wa);
+                    if (DUAL) widen(src + C::Q_BYTES, r, hh, kq, wb);
                     if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&cempty[cst]), cph ^ 1, abort_flag))) {
                         ok = false;
                         break;
                     }
-                    uint8_t* dst = conv + cst * C::CONV_BYTES + r * 128;
-                    widen(src, dst, r, hh, h);
-                    if (DUAL) widen(src + C::Q_BYTES, dst + C::CONV_TILE, r, hh, h);
-                    // generic-proxy writes, read next by the tensor core (async proxy)
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_after();
+                    const uint32_t dst = lane_base + cst * C::A_COLS;
+                    tmem_st16(dst, wa);
+                    if (DUAL) tmem_st16(dst + W8_BK / 2, wb);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&cfull[cst]));
                     if (++cst == C::CSTAGES) { cst = 0; cph ^= 1; }
@@ -361,7 +386,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        tmem_dealloc(tmem_base, W8_TMEM_COLS);
     }
 }
 
