@@ -1,7 +1,8 @@
 """Parity of the CUDA path (through the C ABI) with the oracle, on the same
 seeded inputs, at sizes the oracle finishes in seconds that still span several
-tiles and ragged tails, and on every kernel path (CUDA-core row-dot for <= 8
-tokens, swapped tensor-core GEMM for <= 128, tensor-core GEMM above)."""
+tiles and ragged tails, and on every kernel path (CUDA-core row-dot for one bf16
+token and for fp32, swapped tensor-core GEMM for 2..128 bf16 tokens, tensor-core
+GEMM above)."""
 import numpy as np
 import pytest
 import torch

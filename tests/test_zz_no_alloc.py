@@ -42,10 +42,11 @@ def _call_static(X, Wg, Wu, Wd, tp, Y, P):
                                                 tpl.BF16, tpl.F32 if Y.dtype == torch.float32 else tpl.BF16, stream)
 
 
-# Qwen2.5-1.5B-shaped MLP at decode batch sizes: B = 8 runs the CUDA-core
-# kernel with split-K partials in the scratch, B = 32 the swapped tensor-core
-# GEMM with its split partials, B = 200 the tensor-core GEMM with H in scratch.
-@pytest.mark.parametrize("B", [8, 32, 200])
+# Qwen2.5-1.5B-shaped MLP at decode batch sizes: B = 1 runs the CUDA-core
+# kernel with split-K partials in the scratch, B = 8 and 32 the swapped
+# tensor-core GEMM with its split partials, B = 200 the tensor-core GEMM with H
+# in scratch.
+@pytest.mark.parametrize("B", [1, 8, 32, 200])
 def test_static_scratch_matches_workspace_entry_point(B):
     D, F, tp = 1536, 8960, 2
     Wg = si.normal((F, D), 0.02, 11, "na.Wg", device="cuda")
