@@ -306,9 +306,10 @@ tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void* const* Wq
  *   tpl_tp_mlp_forward_w8_workspace bytes (TPL_ERR_WORKSPACE; nothing in it
  *   needs to start at zero); outputs and ws disjoint from the inputs
  *   (TPL_ERR_ALIAS); the sm_103 tensor-core path (TPL_ERR_UNSUPPORTED).
- *   The int8 tiles are widened to bf16 on the chip and multiplied on the
- *   tensor cores; every int8 value is a bf16 value, so only the accumulation
- *   order differs from the bf16 call.  Asynchronous on `stream`.
+ *   One or two tokens run on CUDA cores (fp32 FMAs); more run on the tensor
+ *   cores, the int8 tiles widened to bf16 on the chip.  Every int8 value is a
+ *   bf16 value, so only the accumulation order differs from the bf16 call.
+ *   Asynchronous on `stream`.
  * ------------------------------------------------------------------------ */
 tpl_status tpl_quantize_w8(const void* W, int64_t rows, int64_t cols, int groups, int8_t* Q,
                            float* scale, void* stream);

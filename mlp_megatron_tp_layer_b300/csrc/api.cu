@@ -765,15 +765,24 @@ extern "C" tpl_status tpl_tp_decoder_layer(const void* x, void* y, const void* W
 
 namespace {
 struct W8Plan {
+    bool rowdot;    // few tokens: CUDA-core kernel (see launch_w8_rowdot), else tensor cores
     KSplit ks_gu;   // gate/up: K = D, one shard, split into chunks to fill the machine
     KSplit ks_d;    // down: K = F, tp shards, each split into chunks
     size_t h_off, gu_off, gu2_off, part_off, total;
 };
 W8Plan plan_mlp_w8(int64_t B, int64_t D, int64_t F, int tp) {
     W8Plan p{};
-    const int64_t ntok = (B + 127) / 128;
-    p.ks_gu = choose_split((F + 127) / 128 * ntok, D, 1, 256, 64);
-    p.ks_d = choose_split((D + 127) / 128 * ntok, F / tp, tp, 256, 64);
+    p.rowdot = B <= kW8RowdotMaxTokens;
+    if (p.rowdot) {
+        // row-dot blocks cover 16 (gate/up pairs) or 32 (down) features; about
+        // four blocks share an SM
+        p.ks_gu = choose_split(std::max<int64_t>(1, (F + 15) / 16 / 4), D, 1, 512, 64);
+        p.ks_d = choose_split(std::max<int64_t>(1, (D + 31) / 32 / 4), F / tp, tp, 512, 64);
+    } else {
+        const int64_t ntok = (B + 127) / 128;
+        p.ks_gu = choose_split((F + 127) / 128 * ntok, D, 1, 256, 64);
+        p.ks_d = choose_split((D + 127) / 128 * ntok, F / tp, tp, 256, 64);
+    }
     p.h_off = 0;
     p.gu_off = up((size_t)B * F * 2);
     const size_t gu = p.ks_gu.sub > 1 ? up((size_t)p.ks_gu.sub * B * F * 4) : 0;
@@ -856,9 +865,10 @@ extern "C" tpl_status tpl_tp_mlp_forward_w8(const void* X, const int8_t* Qg, con
         g.epi.mode = EPI_PARTIAL2; g.epi.out32 = gp; g.epi.out32b = up_p; g.epi.ldo = F;
         g.epi.split_stride = B * F;
     }
+    auto gemm = p.rowdot ? launch_w8_rowdot : launch_w8_gemm;
     {
         ProfScope prof("w8_gateup", st);
-        if (launch_w8_gemm(g, st) != cudaSuccess) return TPL_ERR_CUDA;
+        if (gemm(g, st) != cudaSuccess) return TPL_ERR_CUDA;
     }
     if (p.ks_gu.sub > 1) {
         // SwiGLU of the chunk sums (chunks added in K order), stored bf16
@@ -875,7 +885,7 @@ extern "C" tpl_status tpl_tp_mlp_forward_w8(const void* X, const int8_t* Qg, con
     d.epi = epi_partial(part, D, B * D);
     {
         ProfScope prof("w8_down", st);
-        if (launch_w8_gemm(d, st) != cudaSuccess) return TPL_ERR_CUDA;
+        if (gemm(d, st) != cudaSuccess) return TPL_ERR_CUDA;
     }
     return cuda_status(reduce_into(part, B, D, p.ks_d, partials, Y, out_dtype == TPL_BF16, TPL_ALLREDUCE, nullptr,
                                    nullptr, nullptr, st));

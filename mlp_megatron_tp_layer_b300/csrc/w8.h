@@ -27,4 +27,9 @@ struct W8GemmArgs {
 };
 cudaError_t launch_w8_gemm(const W8GemmArgs& a, cudaStream_t st);
 
+// The same product on CUDA cores for at most kW8RowdotMaxTokens tokens (fp32
+// FMAs on the exactly widened codes); same arguments and epilogues.
+constexpr int kW8RowdotMaxTokens = 2;
+cudaError_t launch_w8_rowdot(const W8GemmArgs& a, cudaStream_t st);
+
 }  // namespace tpl

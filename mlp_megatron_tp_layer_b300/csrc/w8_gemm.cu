@@ -71,8 +71,13 @@ struct W8Cfg {
     static constexpr int RAW_BYTES = X_BYTES + NA * Q_BYTES;
     static constexpr int STAGES_RAW = (200 * 1024) / RAW_BYTES;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-    // TMEM: accumulators (two if they fit beside four operand stages), then operand stages
-    static constexpr int ACC_COLS = DUAL ? 2 * BN : BN;
+    // TMEM: accumulators (two if they fit beside four operand stages), then operand stages.
+    // Consecutive MMAs into one accumulator wait for each other, and a narrow
+    // (N = 16, 32) MMA is short next to that wait, so narrow tiles spread their
+    // K slices over NCHAIN independent accumulators that the epilogue adds up.
+    static constexpr int NCHAIN = BN <= 16 ? 4 : (BN <= 32 ? 2 : 1);
+    static constexpr int ACC1 = DUAL ? 2 * BN : BN;               // one chain: [gate | up] or [out]
+    static constexpr int ACC_COLS = NCHAIN * ACC1;
     static constexpr int A_COLS = NA * (W8_BK / 2);               // 64 bf16 = 32 columns per operand
     static constexpr int NACC = (2 * ACC_COLS + 4 * A_COLS <= W8_TMEM_COLS) ? 2 : 1;
     static constexpr int A_BASE = NACC * ACC_COLS;
@@ -274,10 +279,13 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         const uint32_t sb = smem_addr(raw + stage * C::RAW_BYTES + hh * C::X_HALF);
 #pragma unroll
                         for (int kk = 0; kk < W8_BK / 16; ++kk) {
-                            const uint32_t accum = (kb | hh | kk) ? 1u : 0u;
+                            // K slice kk goes to chain kk % NCHAIN; each chain starts from zero
+                            const int j = kk % C::NCHAIN;
+                            const uint32_t accum = (kb == 0 && hh == 0 && kk < C::NCHAIN) ? 0u : 1u;
+                            const uint32_t dj = d + j * C::ACC1;
                             // K = 16 bf16 per instruction: 8 TMEM columns of A, 32 bytes of the B row
-                            mma_bf16_ta(d, a + kk * 8, sw128_desc(sb + kk * 32), idesc, accum);
-                            if (DUAL) mma_bf16_ta(d + BN, a + W8_BK / 2 + kk * 8, sw128_desc(sb + kk * 32), idesc,
+                            mma_bf16_ta(dj, a + kk * 8, sw128_desc(sb + kk * 32), idesc, accum);
+                            if (DUAL) mma_bf16_ta(dj + BN, a + W8_BK / 2 + kk * 8, sw128_desc(sb + kk * 32), idesc,
                                                   accum);
                         }
                         mma_commit(smem_addr(&cempty[cst]));
@@ -316,11 +324,29 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (DUAL) sc2 = p.scale2[f * p.groups + grp];
             }
             constexpr int CH = BN >= 32 ? 32 : 16;
-            float v[32], u[32];
+            float v[32], u[32], t2[32];
+            auto ld = [&](uint32_t addr, float (&dst)[32]) {
+                if (CH == 32) tmem_ld32(addr, dst); else tmem_ld16(addr, dst);
+            };
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += CH) {
-                if (CH == 32) tmem_ld32(tbase + c0, v); else tmem_ld16(tbase + c0, v);
-                if (DUAL) { if (CH == 32) tmem_ld32(tbase + BN + c0, u); else tmem_ld16(tbase + BN + c0, u); }
+                // the chains' sums, added in chain order
+                ld(tbase + c0, v);
+#pragma unroll 1
+                for (int j = 1; j < C::NCHAIN; ++j) {
+                    ld(tbase + j * C::ACC1 + c0, t2);
+#pragma unroll
+                    for (int e = 0; e < CH; ++e) v[e] += t2[e];
+                }
+                if (DUAL) {
+                    ld(tbase + BN + c0, u);
+#pragma unroll 1
+                    for (int j = 1; j < C::NCHAIN; ++j) {
+                        ld(tbase + j * C::ACC1 + BN + c0, t2);
+#pragma unroll
+                        for (int e = 0; e < CH; ++e) u[e] += t2[e];
+                    }
+                }
                 if (f < p.M) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
@@ -427,6 +453,151 @@ quantize_w8_kernel(const __nv_bfloat16* __restrict__ W, int64_t rows, int64_t co
     if (lane == 0) scale[gid] = s;
 }
 
+// ------------------------------------------------ CUDA-core int8 row-dot
+// For one or two tokens the tensor cores are the wrong tool: a tcgen05.mma of
+// M = 128, K = 16 takes about as long at N = 16 as at N = 256 (about 0.1 us,
+// measured), which caps the swapped GEMM near 2e10 weights per second per SM --
+// the bf16 stream rate, so int8 gains nothing there.  This kernel streams the
+// codes with 16-byte loads, widens them with the same exact trick and does
+// fp32 FMAs: about three instructions per weight and token.  Measured on the
+// Llama-3.1-70B-shaped MLP: 181 us at one token against 229 us for bf16; at
+// four tokens its FMAs and registers make it slower than the tensor cores.
+//
+// Each warp owns RW output features (rows of Q; with DUAL the same rows of Q
+// and Q2) over one K split; lanes stride over K in 16-weight vectors, U vectors
+// per lane in flight per row; the warp's sums are reduced with shuffles,
+// scaled, and stored by distinct lanes.
+constexpr int W8R_WARPS = 8;
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// 16 int8 codes -> 16 exact floats (see widen).
+__device__ __forceinline__ void codes_to_f32(const uint4& v, float (&f)[16]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = w[i] ^ 0x80808080u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            f[4 * i + e] = __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7540 + e)) - 8388736.0f;
+    }
+}
+
+struct W8RowdotArgs {
+    const int8_t* Q; const int8_t* Q2;
+    const float* scale; const float* scale2;
+    int groups;
+    int64_t M, K;
+    const __nv_bfloat16* X; int64_t ldx; int nb;
+    KSplit ks;
+    Epilogue epi;
+};
+
+template <int NB, int RW, bool DUAL>
+__global__ void __launch_bounds__(W8R_WARPS * 32) w8_rowdot_kernel(const W8RowdotArgs a) {
+    constexpr int R = DUAL ? 2 * RW : RW;
+    constexpr int U = 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t f0 = ((int64_t)blockIdx.x * W8R_WARPS + warp) * RW;
+    if (f0 >= a.M) return;
+    const int split = blockIdx.y;
+    const int sh = split / a.ks.sub, j = split - sh * a.ks.sub;
+    const int64_t kbeg = sh * a.ks.k_shard + (int64_t)j * a.ks.k_chunk;
+    const int64_t kend = min(kbeg + a.ks.k_chunk, (int64_t)(sh + 1) * a.ks.k_shard);
+
+    const int8_t* wp[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = min(f0 + (r % RW), a.M - 1);
+        wp[r] = ((DUAL && r >= RW) ? a.Q2 : a.Q) + row * a.K;
+    }
+    float acc[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+
+    for (int64_t k = kbeg + lane * 16; k < kend; k += 32 * 16 * U) {
+        uint4 wv[U][R];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t kk = k + u * 32 * 16;
+#pragma unroll
+            for (int r = 0; r < R; ++r) wv[u][r] = kk < kend ? ld_stream16(wp[r] + kk) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t kk = k + u * 32 * 16;
+            if (kk >= kend) break;
+            float xf[NB][16];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b < a.nb) {
+                    const __nv_bfloat16* xp = a.X + (int64_t)b * a.ldx + kk;
+                    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(xp));
+                    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(xp + 8));
+                    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        xf[b][2 * i] = __uint_as_float(w[i] << 16);
+                        xf[b][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) xf[b][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float wf[16];
+                codes_to_f32(wv[u][r], wf);
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[r][b] = fmaf(wf[e], xf[b][e], acc[r][b]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[r][b] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][b], o);
+        }
+    const int grp = a.groups > 1 ? sh : 0;
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int idx = r * NB + b;
+            const int64_t f = f0 + r;
+            if (lane == (idx & 31) && b < a.nb && f < a.M) {
+                const float sc = a.scale[f * a.groups + grp];
+                if (DUAL)
+                    store_pair(a.epi, split, b, f, acc[r][b] * sc, acc[r + RW][b] * a.scale2[f * a.groups + grp]);
+                else
+                    store_value(a.epi, split, b, f, acc[r][b] * sc);
+            }
+        }
+    }
+}
+
+template <bool DUAL>
+cudaError_t launch_w8_rowdot_t(const W8RowdotArgs& a, cudaStream_t st) {
+    constexpr int RW = DUAL ? 2 : 4;
+    dim3 grid((unsigned)((a.M + W8R_WARPS * RW - 1) / (W8R_WARPS * RW)), (unsigned)(a.ks.tp * a.ks.sub));
+    dim3 block(W8R_WARPS * 32);
+    if (a.nb <= 1) w8_rowdot_kernel<1, RW, DUAL><<<grid, block, 0, st>>>(a);
+    else w8_rowdot_kernel<2, RW, DUAL><<<grid, block, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -518,6 +689,18 @@ cudaError_t launch_w8_gemm(const W8GemmArgs& a, cudaStream_t st) {
     if (a.N <= 32) return dual ? launch_cfg<32, true>(a, st) : launch_cfg<32, false>(a, st);
     if (a.N <= 64) return dual ? launch_cfg<64, true>(a, st) : launch_cfg<64, false>(a, st);
     return dual ? launch_cfg<128, true>(a, st) : launch_cfg<128, false>(a, st);
+}
+
+cudaError_t launch_w8_rowdot(const W8GemmArgs& g, cudaStream_t st) {
+    if (g.N > kW8RowdotMaxTokens) return cudaErrorInvalidValue;
+    W8RowdotArgs a{};
+    a.Q = g.Q; a.Q2 = g.Q2; a.scale = g.scale; a.scale2 = g.scale2; a.groups = g.groups;
+    a.M = g.M; a.K = g.K;
+    a.X = static_cast<const __nv_bfloat16*>(g.X); a.ldx = g.ldx; a.nb = (int)g.N;
+    a.ks = g.ks;
+    a.epi = g.epi;
+    const bool dual = g.epi.mode == EPI_SWIGLU || g.epi.mode == EPI_PARTIAL2;
+    return dual ? launch_w8_rowdot_t<true>(a, st) : launch_w8_rowdot_t<false>(a, st);
 }
 
 cudaError_t launch_quantize_w8(const void* W, int64_t rows, int64_t cols, int groups, int8_t* Q, float* scale,

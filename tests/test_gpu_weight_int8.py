@@ -6,8 +6,9 @@
   (every int8 code is a bf16 value, so only the fp32 accumulation order
   differs): the stated bar, max|err| <= 1e-2 * rms, against the oracle's
   sharded MLP on q * s, for the output and for every shard's partial sum --
-  at sizes that span several tiles, both token-tile widths, split K and
-  ragged token counts, and at full Qwen2.5-1.5B / Llama-3.1-70B width on
+  on both kernels (CUDA-core row-dot for one or two tokens, tensor cores
+  above), at sizes that span several tiles, both token-tile widths, split K
+  and ragged token counts, and at full Qwen2.5-1.5B / Llama-3.1-70B width on
   sampled rows.
 """
 import numpy as np
@@ -61,7 +62,9 @@ def test_quantiser_ties_go_to_even():
 
 
 @pytest.mark.parametrize("B,D,F,tp", [
-    (1, 256, 1024, 2),       # 16-token tile, split K on both projections
+    (1, 256, 1024, 2),       # CUDA-core row-dot (one token), split K on both projections
+    (2, 512, 1536, 4),       # CUDA-core row-dot, two tokens
+    (3, 256, 1024, 2),       # tensor cores, 16-token tile
     (5, 512, 1536, 4),
     (40, 256, 2048, 2),      # 64-token tile with 24 padded columns
     (17, 192, 768, 3),       # 32-token tile, three shards
@@ -95,6 +98,7 @@ def test_w8_mlp_tracks_bf16_mlp_and_is_deterministic():
 @pytest.mark.parametrize("name,D,F,tp,B", [
     ("qwen2.5-1.5b", 1536, 8960, 2, 64),
     ("llama-3.1-70b", 8192, 28672, 8, 8),
+    ("llama-3.1-70b", 8192, 28672, 8, 1),
 ])
 def test_w8_mlp_full_width_sampled_rows(name, D, F, tp, B):
     """Full model width, in the launch configuration the benchmark times; the
