@@ -67,7 +67,9 @@ def args_parse():
     ap.add_argument("--model", "--lm-head-model", dest="model", choices=["llama-3.1-70b", "qwen2.5-1.5b"],
                     default=None, help="with --only lm_head or --only w8: one model's shape only "
                                        "(--batches selects the batch sizes)")
-    ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head", "w8"], default=None,
+    ap.add_argument("--llama-layers", type=int, default=LD["n_layers"],
+                    help="layers of the Llama-3.1-70B-shaped decode stack (small captures)")
+    ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head", "w8", "cases"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
     ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
@@ -458,8 +460,11 @@ def run_parallel_block(args, tpl, dev, layers, peaks, stream):
 def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
     """Llama-3.1-70B-shaped decode stack (8 layers, TP=8, 13.69 GB of weights),
     one graph-replayed forward per batch size: weight-stream GB/s per batch."""
-    D, F, n_q, n_kv, hd, tp, L = LD["D"], LD["F"], LD["n_q"], LD["n_kv"], LD["head_dim"], LD["tp"], LD["n_layers"]
+    D, F, n_q, n_kv, hd, tp = LD["D"], LD["F"], LD["n_q"], LD["n_kv"], LD["head_dim"], LD["tp"]
+    L = args.llama_layers
     batches = list(LD["batches"])
+    if args.only == "llama" and args.batches:
+        batches = [int(b) for b in args.batches.split(",")]
     layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=0, layer=l, prefix="llama", device=dev) for l in range(L)]
     xs = {B: si.activations(B, D, seed=3, name=f"llama.x{B}", device=dev) for B in batches}
     ys = {B: torch.empty_like(xs[B]) for B in batches}
@@ -741,6 +746,12 @@ def main():
         lm = run_lm_head(args, tpl, dev, peaks, stream)
         if rank == 0:
             print(json.dumps(dict(lm_head=lm, metric=METRIC, n_gpus=world, steps=args.steps)), flush=True)
+        return
+    if args.only == "cases":
+        cases, reduce_line = run_cases_and_reduce(args, tpl, dev, peaks, peak_kind)
+        if rank == 0:
+            print(json.dumps(dict(sharded_matmul=cases, shard_reduce=reduce_line, metric=METRIC, n_gpus=world,
+                                  steps=args.steps)), flush=True)
         return
     if args.only == "llama":
         ll = run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream)
