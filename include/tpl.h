@@ -357,7 +357,9 @@ tpl_status tpl_vocab_parallel_topk(const void* X, const void* W, int64_t B, int6
  * tpl_profile_enable(n > 0) creates n pairs of CUDA events (host objects; no
  * device memory) and from then on brackets each kernel launch with a pair on
  * the launch's stream, tagged with the step it implements ("qkv", "oproj",
- * "gateup", "down", "matmul", "reduce", "reduce_norm", "rmsnorm").  Launches
+ * "gateup", "down", "matmul", "reduce", "reduce_norm", "rmsnorm",
+ * "fused_stack", "lm_head_topk" (both lm_head kernels), "quantize_w8",
+ * "w8_gateup", "w8_down").  Launches
  * beyond n are not recorded.  tpl_profile_enable(0) turns it off and frees the
  * events.  tpl_profile_count() is the number of recorded launches;
  * tpl_profile_read(i, ...) waits for launch i and returns its tag and its

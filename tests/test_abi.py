@@ -12,9 +12,23 @@ NULL = None
 
 def test_every_declared_symbol_is_exported():
     names = tpl.header_functions()
-    assert len(names) >= 13
+    assert len(names) >= 24
     missing = [n for n in names if not hasattr(lib, n)]
     assert missing == []
+
+
+def test_binding_declares_every_header_function_with_its_arity():
+    """The ctypes table covers the whole header, argument count for argument
+    count, so no call goes through ctypes' default int conversion."""
+    import re
+    text = open(tpl.HEADER).read()
+    for name in tpl.header_functions():
+        assert name in tpl._SIGS, name
+        m = re.search(r"\b%s\s*\(([^;]*?)\)\s*;" % name, text, re.S)
+        assert m, name
+        params = m.group(1).strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(tpl._SIGS[name][1]) == n, (name, n, len(tpl._SIGS[name][1]))
 
 
 def test_status_strings_and_version():
