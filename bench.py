@@ -221,19 +221,33 @@ def cpu_baseline(layers_dev, budget_s):
     W = {k: v.to("cpu", torch.float64).numpy() for k, v in layers_dev[0].items()}
     xs = {B: si.activations(B, QW["D"], seed=1, name=f"bench.x{B}").to(torch.float64).numpy()
           for B in QW["batches"]}
-    n = 0
-    t0 = time.perf_counter()
-    while True:
-        for B in QW["batches"]:
-            O.decoder_layer(xs[B], W, QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"])
-            n += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
+    def timed(budget):
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            for B in QW["batches"]:
+                O.decoder_layer(xs[B], W, QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"])
+                n += 1
+            if time.perf_counter() - t0 > budget:
+                break
+        return n, time.perf_counter() - t0
+
+    n, dt = timed(budget_s)
+    single = None
+    try:
+        # the same oracle on one host thread (a quarter of the budget)
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            n1, dt1 = timed(budget_s / 4)
+        single = n1 * QWEN_LAYER_BYTES / dt1 / 1e9
+    except Exception:  # noqa: BLE001
+        pass
     del np
     return {"value": n * QWEN_LAYER_BYTES / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread_value": single,
             "sample": f"{n // len(QW['batches'])} passes of one Qwen-shaped TP=2 layer over B in "
-                      f"{list(QW['batches'])} (numpy float64), {dt:.1f} s"}
+                      f"{list(QW['batches'])} (numpy float64), {dt:.1f} s; then one thread for a quarter "
+                      f"of that budget"}
 
 
 def run_reference(args, rank, world):
