@@ -72,10 +72,10 @@ struct W8Cfg {
     static constexpr int STAGES_RAW = (200 * 1024) / RAW_BYTES;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     // TMEM: accumulators (two if they fit beside four operand stages), then operand stages.
-    // Consecutive MMAs into one accumulator wait for each other, and a narrow
-    // (N = 16, 32) MMA is short next to that wait, so narrow tiles spread their
-    // K slices over NCHAIN independent accumulators that the epilogue adds up.
-    static constexpr int NCHAIN = BN <= 16 ? 4 : (BN <= 32 ? 2 : 1);
+    // NCHAIN > 1 would spread the K slices over independent accumulators that
+    // the epilogue adds up; measured back to back, MMAs into one accumulator run
+    // as fast as into four, so one chain is used.
+    static constexpr int NCHAIN = 1;
     static constexpr int ACC1 = DUAL ? 2 * BN : BN;               // one chain: [gate | up] or [out]
     static constexpr int ACC_COLS = NCHAIN * ACC1;
     static constexpr int A_COLS = NA * (W8_BK / 2);               // 64 bf16 = 32 columns per operand
@@ -454,10 +454,10 @@ quantize_w8_kernel(const __nv_bfloat16* __restrict__ W, int64_t rows, int64_t co
 }
 
 // ------------------------------------------------ CUDA-core int8 row-dot
-// For one or two tokens the tensor cores are the wrong tool: a tcgen05.mma of
-// M = 128, K = 16 takes about as long at N = 16 as at N = 256 (about 0.1 us,
-// measured), which caps the swapped GEMM near 2e10 weights per second per SM --
-// the bf16 stream rate, so int8 gains nothing there.  This kernel streams the
+// For one or two tokens the tensor-core kernel above is the wrong tool: it
+// streams only about 2e10 weights per second per SM -- its pipeline advances
+// one 64-wide K half every 0.77 us, of which the eight MMAs themselves take
+// about 0.23 us -- so int8 gains nothing over bf16 there.  This kernel streams the
 // codes with 16-byte loads, widens them with the same exact trick and does
 // fp32 FMAs: about three instructions per weight and token.  Measured on the
 // Llama-3.1-70B-shaped MLP: 181 us at one token against 229 us for bf16; at
