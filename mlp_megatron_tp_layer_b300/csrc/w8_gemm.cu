@@ -107,6 +107,22 @@ __device__ __forceinline__ void split_range(const W8Params& p, int sp, int64_t& 
     nkb = (int)((k1 - k0 + W8_BK - 1) / W8_BK);
 }
 
+// Non-blocking test of a phase, then the bounded wait only if it has not
+// completed.  Most waits of the MMA warp find their phase long complete, and
+// the test costs a fraction of the blocking try-wait and its call.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool fast_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_test(bar, parity) || mbar_wait(bar, parity, abort_flag);
+}
+
 // tcgen05.mma with the A operand in tensor memory (kind::f16, bf16 x bf16 -> fp32).
 __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -224,7 +240,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const int bn = c.nt * BN;
                 for (int kb = 0; kb < nkb; kb += 2) {
                     const int halves = min(2, nkb - kb);
-                    if (!mbar_wait(smem_addr(&empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+                    if (!fast_wait(smem_addr(&empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
                     const uint32_t fb = smem_addr(&full[stage]);
                     mbar_expect_tx(fb, C::NA * C::Q_BYTES + halves * C::X_HALF);
                     uint8_t* st = raw + stage * C::RAW_BYTES;
@@ -264,19 +280,25 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 split_range(p, c.sp, k0, nkb);
                 const int acc = it % C::NACC;
                 const uint32_t acc_phase = (it / C::NACC) & 1;
-                if (!mbar_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!fast_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * C::ACC_COLS;
                 for (int kb = 0; kb < nkb && ok; kb += 2) {
                     const int halves = min(2, nkb - kb);
                     for (int hh = 0; hh < halves; ++hh) {
                         // widened weights in TMEM (the converters saw the stage land);
-                        // the token tiles' own barrier is already complete by then
-                        if (!mbar_wait(smem_addr(&cfull[cst]), cph, abort_flag) ||
-                            !mbar_wait(smem_addr(&full[stage]), phase, abort_flag)) { ok = false; break; }
+                        // the token tiles' own barrier is already complete by then and
+                        // is observed once per stage
+                        if (!fast_wait(smem_addr(&cfull[cst]), cph, abort_flag) ||
+                            (hh == 0 && !fast_wait(smem_addr(&full[stage]), phase, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
                         const uint32_t a = tmem_base + C::A_BASE + cst * C::A_COLS;
-                        const uint32_t sb = smem_addr(raw + stage * C::RAW_BYTES + hh * C::X_HALF);
+                        // descriptor of the token tile; each 16-wide K slice starts 32 bytes
+                        // further, i.e. 2 in the descriptor's address field
+                        const uint64_t bdesc = sw128_desc(smem_addr(raw + stage * C::RAW_BYTES + hh * C::X_HALF));
 #pragma unroll
                         for (int kk = 0; kk < W8_BK / 16; ++kk) {
                             // K slice kk goes to chain kk % NCHAIN; each chain starts from zero
@@ -284,9 +306,8 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             const uint32_t accum = (kb == 0 && hh == 0 && kk < C::NCHAIN) ? 0u : 1u;
                             const uint32_t dj = d + j * C::ACC1;
                             // K = 16 bf16 per instruction: 8 TMEM columns of A, 32 bytes of the B row
-                            mma_bf16_ta(dj, a + kk * 8, sw128_desc(sb + kk * 32), idesc, accum);
-                            if (DUAL) mma_bf16_ta(dj + BN, a + W8_BK / 2 + kk * 8, sw128_desc(sb + kk * 32), idesc,
-                                                  accum);
+                            mma_bf16_ta(dj, a + kk * 8, bdesc + 2 * kk, idesc, accum);
+                            if (DUAL) mma_bf16_ta(dj + BN, a + W8_BK / 2 + kk * 8, bdesc + 2 * kk, idesc, accum);
                         }
                         mma_commit(smem_addr(&cempty[cst]));
                         if (++cst == C::CSTAGES) { cst = 0; cph ^= 1; }
@@ -378,7 +399,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             split_range(p, c.sp, k0, nkb);
             for (int kb = 0; kb < nkb && ok; kb += 2) {
                 const int halves = min(2, nkb - kb);
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[stage]), phase, abort_flag))) {
+                if (!__all_sync(0xFFFFFFFFu, fast_wait(smem_addr(&full[stage]), phase, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -387,7 +408,7 @@ w8_gemm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     uint32_t wa[16], wb[16];
                     widen(src, r, hh, kq, wa);
                     if (DUAL) widen(src + C::Q_BYTES, r, hh, kq, wb);
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&cempty[cst]), cph ^ 1, abort_flag))) {
+                    if (!__all_sync(0xFFFFFFFFu, fast_wait(smem_addr(&cempty[cst]), cph ^ 1, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -454,10 +475,9 @@ quantize_w8_kernel(const __nv_bfloat16* __restrict__ W, int64_t rows, int64_t co
 }
 
 // ------------------------------------------------ CUDA-core int8 row-dot
-// For one or two tokens the tensor-core kernel above is the wrong tool: it
-// streams only about 2e10 weights per second per SM -- its pipeline advances
-// one 64-wide K half every 0.77 us, of which the eight MMAs themselves take
-// about 0.23 us -- so int8 gains nothing over bf16 there.  This kernel streams the
+// For one or two tokens the tensor-core kernel above is the wrong tool: its
+// MMA warp issues eight MMAs plus barrier checks per 64-wide K half, which
+// holds it near the bf16 weight rate, so int8 gains little there.  This kernel streams the
 // codes with 16-byte loads, widens them with the same exact trick and does
 // fp32 FMAs: about three instructions per weight and token.  Measured on the
 // Llama-3.1-70B-shaped MLP: 181 us at one token against 229 us for bf16; at
