@@ -107,20 +107,10 @@ __device__ __forceinline__ void split_range(const W8Params& p, int sp, int64_t& 
     nkb = (int)((k1 - k0 + W8_BK - 1) / W8_BK);
 }
 
-// Non-blocking test of a phase, then the bounded wait only if it has not
-// completed.  Most waits of the MMA warp find their phase long complete, and
-// the test costs a fraction of the blocking try-wait and its call.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
+// The bounded wait, which first tests the phase without blocking (most waits
+// of the MMA warp find their phase long complete).
 __device__ __forceinline__ bool fast_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    return mbar_test(bar, parity) || mbar_wait(bar, parity, abort_flag);
+    return mbar_wait(bar, parity, abort_flag);
 }
 
 // tcgen05.mma with the A operand in tensor memory (kind::f16, bf16 x bf16 -> fp32).
