@@ -237,7 +237,7 @@ def cpu_baseline(layers_dev, budget_s):
     try:
         # the same oracle on one host thread (a quarter of the budget)
         from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
+        with threadpool_limits(limits=1, user_api="blas"):
             n1, dt1 = timed(budget_s / 4)
         single = n1 * QWEN_LAYER_BYTES / dt1 / 1e9
     except Exception:  # noqa: BLE001
