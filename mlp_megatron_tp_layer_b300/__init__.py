@@ -405,6 +405,10 @@ def vocab_parallel_topk(x, W, tp: int, k: int = 1, shard_outputs: bool = False, 
         val = torch.empty(B, k, dtype=torch.float32, device=dev)
     else:
         idx, val = out
+        if (idx.dtype != torch.int32 or val.dtype != torch.float32 or tuple(idx.shape) != (B, k)
+                or tuple(val.shape) != (B, k)):
+            raise ValueError("out must be (int32 [B, k], float32 [B, k])")
+        _contig(idx, val)
     sidx = sval = None
     if shard_outputs:
         sidx = torch.empty(tp, B, k, dtype=torch.int32, device=dev)
@@ -441,6 +445,13 @@ def tp_mlp_forward_w8(X, Qg, sg, Qu, su, Qd, sd, tp: int, out=None, partials=Non
     _contig(X, Qg, sg, Qu, su, Qd, sd)
     B, D = X.shape
     F = Qg.shape[0]
+    # the library reads exactly these many codes and scales
+    if Qg.shape != (F, D) or Qu.shape != (F, D) or Qd.shape != (D, F):
+        raise ValueError("codes must be Qg, Qu [F, D] and Qd [D, F]")
+    if sg.numel() != F or su.numel() != F or sd.numel() != D * tp:
+        raise ValueError("scales must be sg, su [F] (one group) and sd [D, tp] (one per shard)")
+    if any(t.dtype != torch.int8 for t in (Qg, Qu, Qd)) or any(t.dtype != torch.float32 for t in (sg, su, sd)):
+        raise TypeError("codes are int8 and scales float32")
     odt = _out_code(BF16, out, out_dtype)
     if out is None:
         out = torch.empty(B, D, dtype=_tdt(odt), device=X.device)

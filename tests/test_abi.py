@@ -137,3 +137,31 @@ def test_vocab_topk_rejects_bad_arguments_before_any_launch():
     assert call(idx=ctypes.c_void_p((1 << 24) + 64)) == 9    # top_idx inside X
     assert call(val=ctypes.c_void_p((4 << 24) + 16)) == 9    # top_val overlaps top_idx
     assert call(sidx=ctypes.c_void_p((3 << 24) + 256)) == 9  # shard output inside the workspace
+
+
+def test_int8_binding_checks_code_and_scale_shapes_before_calling():
+    """Scales are read by index from the shapes the call implies, so the binding
+    refuses mismatched arrays before anything reaches the library (CPU tensors
+    suffice: nothing is launched)."""
+    import torch
+    B, D, F, tp = 2, 64, 128, 2
+    x = torch.zeros(B, D, dtype=torch.bfloat16)
+    q = lambda r, c: torch.zeros(r, c, dtype=torch.int8)  # noqa: E731
+    f = lambda *s: torch.zeros(*s, dtype=torch.float32)  # noqa: E731
+    good = (q(F, D), f(F, 1), q(F, D), f(F, 1), q(D, F), f(D, tp))
+    with pytest.raises(ValueError):
+        tpl.tp_mlp_forward_w8(x, *good[:5], f(D, 1), tp)           # down scales for one group, not tp
+    with pytest.raises(ValueError):
+        tpl.tp_mlp_forward_w8(x, q(F, D + 64), *good[1:], tp)      # codes wider than X
+    with pytest.raises(TypeError):
+        tpl.tp_mlp_forward_w8(x, good[0].float(), *good[1:], tp)   # codes not int8
+
+
+def test_lm_head_binding_checks_given_outputs():
+    import torch
+    x = torch.zeros(3, 64, dtype=torch.bfloat16)
+    W = torch.zeros(256, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        tpl.vocab_parallel_topk(x, W, 2, 2, out=(torch.zeros(3, 1, dtype=torch.int32), torch.zeros(3, 1)))
+    with pytest.raises(ValueError):
+        tpl.vocab_parallel_topk(x, W, 2, 2, out=(torch.zeros(3, 2), torch.zeros(3, 2)))
