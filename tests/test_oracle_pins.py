@@ -445,3 +445,25 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     with pytest.raises((AssertionError, ValueError)):
         test_head_map_tp1_is_unsharded_and_groups_follow_gqa()
     monkeypatch.setattr(O, "kv_group_of_head", real_g)
+
+
+@pytest.mark.parametrize("D", [16, 32, 48])
+@pytest.mark.parametrize("F", [16, 32, 48])
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_sharded_and_unsharded_agree_over_tiny_shapes(D, F, B):
+    """Every divisor of F as the shard count: the sharded MLP (per-shard H and
+    partials, summed in shard order) equals the unsharded one to fp64
+    rounding, and the partials sum to it exactly on integer data."""
+    r = rng(100 + D + F + B)
+    X = r.standard_normal((B, D))
+    Wg, Wu = r.standard_normal((F, D)) * 0.2, r.standard_normal((F, D)) * 0.2
+    Wd = r.standard_normal((D, F)) * 0.2
+    Y = O.mlp_unsharded(X, Wg, Wu, Wd, bf16=False)
+    Hi = r.integers(-2, 3, (B, F)).astype(float)
+    Wdi = r.integers(-2, 3, (D, F)).astype(float)
+    for tp in [t for t in range(1, F + 1) if F % t == 0]:
+        Ys, P, _ = O.mlp_sharded(X, Wg, Wu, Wd, tp, bf16=False)
+        assert np.allclose(Ys, Y, rtol=1e-12, atol=1e-12)
+        Pi = [O.mlp_partial_shard(Hi[:, O.shard_range(F, tp, s).start:O.shard_range(F, tp, s).stop], Wdi, tp, s)
+              for s in range(tp)]
+        assert np.array_equal(O.shard_reduce(Pi), Hi @ Wdi.T)
