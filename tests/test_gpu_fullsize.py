@@ -92,7 +92,7 @@ def check_layers_against_oracle(x, y, layers, n_q, n_kv, hd, tp, rows, what):
         prev = y_ref
 
 
-@pytest.mark.parametrize("B", [8, 64])
+@pytest.mark.parametrize("B", [1, 8, 32, 64])
 def test_qwen_parallel_block_stack(B):
     """28 Qwen-shaped layers in the parallel arrangement ([L4] S5.5): every layer,
     fed the oracle's own residual stream on sampled rows, matches the oracle's
@@ -121,7 +121,7 @@ def test_qwen_parallel_block_stack(B):
         prev = trace[l]
 
 
-@pytest.mark.parametrize("B", [1, 64])
+@pytest.mark.parametrize("B", [1, 8, 32, 64])
 def test_qwen_decode_stack_as_benchmarked(B):
     """The benchmark's decode step: 28 layers through tp_decoder_stack."""
     D, F, n_q, n_kv, hd, tp, L = QW["D"], QW["F"], QW["n_q"], QW["n_kv"], QW["head_dim"], QW["tp"], QW["n_layers"]
@@ -203,7 +203,7 @@ def test_sharded_cases_full_size(cases_operands, case, mode, gather):
 LD = si.LLAMA_DECODE
 
 
-@pytest.mark.parametrize("B", [1, 128])
+@pytest.mark.parametrize("B", [1, 8, 32, 128])
 def test_llama_decode_layers_full_width(B):
     D, F, n_q, n_kv, hd, tp = LD["D"], LD["F"], LD["n_q"], LD["n_kv"], LD["head_dim"], LD["tp"]
     L = 2

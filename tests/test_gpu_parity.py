@@ -228,7 +228,9 @@ def test_decoder_stack_small(B):
 
 # ------------------------------------------------ fused decode stack
 
-@pytest.mark.parametrize("B", [1, 5, 16, 40, 100, 128])
+# every instantiation of the fused kernel (16, 32, 64 and 128 token columns),
+# at full and ragged batch sizes
+@pytest.mark.parametrize("B", [1, 5, 16, 17, 24, 32, 40, 64, 100, 128])
 @pytest.mark.parametrize("path", [tpl.PATH_FUSED, tpl.PATH_UNFUSED])
 def test_decoder_stack_paths(B, path):
     """Both implementations of the stack against the oracle; each deterministic."""
@@ -262,7 +264,7 @@ def test_decoder_stack_fused_in_place_and_gqa_shapes(B):
 
 # ------------------------------------------ parallel (PaLM) block, [L4] S5.5
 
-@pytest.mark.parametrize("B", [1, 5, 40, 128])
+@pytest.mark.parametrize("B", [1, 5, 17, 32, 40, 64, 128])
 def test_decoder_stack_parallel_block(B):
     """y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)) through the fused stack, against
     the oracle; one bf16 rounding of the residual stream per layer."""
