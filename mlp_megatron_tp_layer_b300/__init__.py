@@ -141,6 +141,54 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous (row-major)")
 
 
+def _need(t, shape, dtype, what: str):
+    """The library reads or writes exactly shape x dtype at t's address: reject
+    a tensor of another shape or type, or not contiguous, before the call (a
+    wrong size would become an out-of-bounds device access)."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous (row-major)")
+
+
+def _same_device(ref, *ts):
+    """Every tensor the call passes lives in ref's CUDA device memory."""
+    if not ref.is_cuda:
+        raise ValueError("tensors must be CUDA tensors")
+    for t in ts:
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"every tensor must be on {ref.device}, got one on {t.device}")
+
+
+def _mlp_args(X, Wg, Wu, Wd, tp, out, partials, out_dtype):
+    """Shape, type and device checks shared by the bf16/fp32 MLP wrappers;
+    returns (B, D, F, dt, odt, out, partials, want_partials)."""
+    _contig(X)
+    if X.dim() != 2 or Wg.dim() != 2:
+        raise ValueError("X must be [B, D] and Wg [F, D]")
+    B, D = X.shape
+    F = Wg.shape[0]
+    dt = _dt(X)
+    for t, shape, name in ((Wg, (F, D), "Wg"), (Wu, (F, D), "Wu"), (Wd, (D, F), "Wd")):
+        _need(t, shape, X.dtype, name)
+    odt = _out_code(dt, out, out_dtype)
+    if out is None:
+        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
+    _need(out, (B, D), _tdt(odt), "out")
+    want = partials is not None and partials is not False
+    if partials is True:
+        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
+    elif not want:
+        partials = None
+    _need(partials, (tp, B, D), torch.float32, "partials")
+    _same_device(X, Wg, Wu, Wd, out, partials)
+    return B, D, F, dt, odt, out, partials, want
+
+
 _ws_cache: dict = {}
 
 
@@ -191,18 +239,7 @@ def tp_mlp_forward(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=No
     ``partials``: None (reduction fused), True (allocate) or an fp32 [tp, B, D] tensor.
     Returns Y, or (Y, partials) when partials were requested.
     """
-    _contig(X, Wg, Wu, Wd)
-    B, D = X.shape
-    F = Wg.shape[0]
-    dt = _dt(X)
-    odt = _out_code(dt, out, out_dtype)
-    if out is None:
-        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
-    want = partials is not None and partials is not False
-    if partials is True:
-        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
-    elif not want:
-        partials = None
+    B, D, F, dt, odt, out, partials, want = _mlp_args(X, Wg, Wu, Wd, tp, out, partials, out_dtype)
     nbytes = mlp_workspace_bytes(B, D, F, tp, dt)
     ws = workspace(nbytes, X.device) if ws is None else ws
     _check(lib.tpl_tp_mlp_forward(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp, dt, odt,
@@ -213,21 +250,13 @@ def tp_mlp_forward(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=No
 def tp_mlp_forward_static_ws(X, Wg, Wu, Wd, tp: int, out=None, partials=None, out_dtype=None, stream=None):
     """tp_mlp_forward with the library's static device scratch instead of a
     workspace: for callers that cannot allocate device memory (see
-    tpl_tp_mlp_forward_static_ws in include/tpl.h for the limit and sharing)."""
-    _contig(X, Wg, Wu, Wd)
-    B, D = X.shape
-    F = Wg.shape[0]
-    dt = _dt(X)
-    odt = _out_code(dt, out, out_dtype)
-    if out is None:
-        out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
-    want = partials is not None and partials is not False
-    if partials is True:
-        partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
-    elif not want:
-        partials = None
-    _check(lib.tpl_tp_mlp_forward_static_ws(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp, dt,
-                                            odt, _stream(stream)), "tpl_tp_mlp_forward_static_ws")
+    tpl_tp_mlp_forward_static_ws in include/tpl.h for the limit and sharing).
+    The call is made with X's device current, since the scratch array the
+    library picks is the current device's."""
+    B, D, F, dt, odt, out, partials, want = _mlp_args(X, Wg, Wu, Wd, tp, out, partials, out_dtype)
+    with torch.cuda.device(X.device):
+        _check(lib.tpl_tp_mlp_forward_static_ws(_p(X), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(partials), B, D, F, tp,
+                                                dt, odt, _stream(stream)), "tpl_tp_mlp_forward_static_ws")
     return (out, partials) if want else out
 
 
@@ -250,22 +279,29 @@ def tp_attn_proj(X, Wqkv, Wo, n_q, n_kv, head_dim, tp, out=None, qkv_out=None, p
     ``qkv_out``: None, True (allocate [tp, B, W_s]) or a tensor.  ``partials`` as in
     tp_mlp_forward.  Returns Y, plus qkv_out / partials when requested (in that order).
     """
-    _contig(X, Wqkv, Wo)
+    _contig(X)
     B, D = X.shape
     dt = _dt(X)
+    _need(Wqkv, ((n_q + 2 * n_kv) * head_dim, D), X.dtype, "Wqkv")
+    _need(Wo, (D, n_q * head_dim), X.dtype, "Wo")
     odt = _out_code(dt, out, out_dtype)
     if out is None:
         out = torch.empty((B, D), dtype=_tdt(odt), device=X.device)
+    _need(out, (B, D), _tdt(odt), "out")
     want_qkv = qkv_out is not None and qkv_out is not False
     if qkv_out is True:
         qkv_out = torch.empty((tp, B, qkv_shard_width(n_q, n_kv, head_dim, tp)), dtype=X.dtype, device=X.device)
     elif not want_qkv:
         qkv_out = None
+    if qkv_out is not None and tp > 0 and n_q % tp == 0:
+        _need(qkv_out, (tp, B, qkv_shard_width(n_q, n_kv, head_dim, tp)), X.dtype, "qkv_out")
     want_p = partials is not None and partials is not False
     if partials is True:
         partials = torch.empty((tp, B, D), dtype=torch.float32, device=X.device)
     elif not want_p:
         partials = None
+    _need(partials, (tp, B, D), torch.float32, "partials")
+    _same_device(X, Wqkv, Wo, out, qkv_out, partials)
     nbytes = attn_workspace_bytes(B, D, n_q, n_kv, head_dim, tp, dt)
     ws = workspace(nbytes, X.device) if ws is None else ws
     _check(lib.tpl_tp_attn_proj(_p(X), _p(Wqkv), _p(Wo), _p(qkv_out), _p(out), _p(partials), B, D, n_q, n_kv,
@@ -292,20 +328,25 @@ def sharded_matmul(case: int, A, Bt, X: int, mode: int = ALLREDUCE, gather: int 
 
     K-sharded results (case 3 reduce-scatter, case 4 gather-A) are [X, I, K/X].
     """
-    _contig(A, Bt)
+    _contig(A)
     I, J = A.shape
     K = Bt.shape[0]
     dt = _dt(A)
+    _need(Bt, (K, J), A.dtype, "Bt")
     odt = _out_code(dt, out, out_dtype)
     k_sharded = (case == 3 and mode == REDUCE_SCATTER) or (case == 4 and gather == GATHER_A)
+    shape = (X, I, K // X) if k_sharded else (I, K)
     if out is None:
-        shape = (X, I, K // X) if k_sharded else (I, K)
         out = torch.empty(shape, dtype=_tdt(odt), device=A.device)
+    if X > 0 and K % X == 0:
+        _need(out, shape, _tdt(odt), "out")
     want_p = partials is not None and partials is not False
     if partials is True:
         partials = torch.empty((X, I, K), dtype=torch.float32, device=A.device)
     elif not want_p:
         partials = None
+    _need(partials, (X, I, K), torch.float32, "partials")
+    _same_device(A, Bt, out, partials)
     nbytes = case_workspace_bytes(case, mode, I, J, K, X, dt)
     ws = workspace(nbytes, A.device) if ws is None else ws
     _check(lib.tpl_sharded_matmul(case, mode, gather, _p(A), _p(Bt), _p(out), _p(partials), I, J, K, X, dt, odt,
@@ -318,6 +359,13 @@ def decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp) -> int:
     _check(lib.tpl_tp_decoder_workspace(B, D, F, n_q, n_kv, head_dim, tp, ctypes.byref(n)),
            "tpl_tp_decoder_workspace")
     return n.value
+
+
+def _layer_args(W, D, F, n_q, n_kv, head_dim, dtype):
+    """Every weight of one decoder layer has the shape the library reads."""
+    for name, shape in (("Wqkv", ((n_q + 2 * n_kv) * head_dim, D)), ("Wo", (D, n_q * head_dim)),
+                        ("Wg", (F, D)), ("Wu", (F, D)), ("Wd", (D, F))):
+        _need(W[name], shape, dtype, name)
 
 
 def _ptr_array(ts):
@@ -333,8 +381,12 @@ def tp_decoder_stack(x, layers, n_q, n_kv, head_dim, tp, out=None, ws=None, stre
     _contig(x)
     B, D = x.shape
     F = layers[0]["Wg"].shape[0]
+    for W in layers:
+        _layer_args(W, D, F, n_q, n_kv, head_dim, x.dtype)
     if out is None:
         out = torch.empty_like(x)
+    _need(out, (B, D), x.dtype, "out")
+    _same_device(x, out, *[W[k] for W in layers for k in ("Wqkv", "Wo", "Wg", "Wu", "Wd")])
     nbytes = decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp)
     ws = workspace(nbytes, x.device) if ws is None else ws
     arrs = [_ptr_array([L[k] for L in layers]) for k in ("Wqkv", "Wo", "Wg", "Wu", "Wd")]
@@ -349,8 +401,11 @@ def tp_decoder_layer(x, W, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=No
     _contig(x)
     B, D = x.shape
     F = W["Wg"].shape[0]
+    _layer_args(W, D, F, n_q, n_kv, head_dim, x.dtype)
     if out is None:
         out = torch.empty_like(x)
+    _need(out, (B, D), x.dtype, "out")
+    _same_device(x, out, *W.values())
     nbytes = decoder_workspace_bytes(B, D, F, n_q, n_kv, head_dim, tp)
     ws = workspace(nbytes, x.device) if ws is None else ws
     _check(lib.tpl_tp_decoder_layer(_p(x), _p(out), _p(W["Wqkv"]), _p(W["Wo"]), _p(W["Wg"]), _p(W["Wu"]),

@@ -165,3 +165,88 @@ def test_lm_head_binding_checks_given_outputs():
         tpl.vocab_parallel_topk(x, W, 2, 2, out=(torch.zeros(3, 1, dtype=torch.int32), torch.zeros(3, 1)))
     with pytest.raises(ValueError):
         tpl.vocab_parallel_topk(x, W, 2, 2, out=(torch.zeros(3, 2), torch.zeros(3, 2)))
+
+
+# ------------------------------------------------ binding argument checks
+# The library reads and writes as much as the sizes imply, so the wrappers
+# reject any tensor of another shape or type before the call.  These checks
+# run before any device is touched, so CPU tensors suffice.
+
+def _t(*shape, dtype=None):
+    import torch
+    return torch.zeros(shape, dtype=dtype or torch.bfloat16)
+
+
+def _mlp(B=4, D=64, F=128):
+    return _t(B, D), _t(F, D), _t(F, D), _t(D, F)
+
+
+def test_mlp_wrappers_reject_wrong_weight_shapes_and_types():
+    import torch
+    for fn in (tpl.tp_mlp_forward, tpl.tp_mlp_forward_static_ws):
+        X, Wg, Wu, Wd = _mlp()
+        with pytest.raises(ValueError, match="Wd"):
+            fn(X, Wg, Wu, _t(128, 64), 2)                      # Wd transposed
+        with pytest.raises(ValueError, match="Wu"):
+            fn(X, Wg, _t(128, 32), Wd, 2)
+        with pytest.raises(TypeError, match="Wg"):
+            fn(X, Wg.float(), Wu, Wd, 2)                       # fp32 weights, bf16 X
+        with pytest.raises(ValueError, match="contiguous"):
+            fn(X, Wg, _t(64, 128).t(), Wd, 2)
+
+
+def test_mlp_wrappers_reject_wrong_outputs():
+    import torch
+    for fn in (tpl.tp_mlp_forward, tpl.tp_mlp_forward_static_ws):
+        X, Wg, Wu, Wd = _mlp()
+        with pytest.raises(ValueError, match="out"):
+            fn(X, Wg, Wu, Wd, 2, out=_t(2, 64))                # smaller than [B, D]
+        with pytest.raises(ValueError, match="partials"):
+            fn(X, Wg, Wu, Wd, 2, partials=_t(2, 4, 32, dtype=torch.float32))
+        with pytest.raises(TypeError, match="partials"):
+            fn(X, Wg, Wu, Wd, 2, partials=_t(2, 4, 64))        # bf16 partials
+        with pytest.raises(ValueError, match="CUDA"):
+            fn(X, Wg, Wu, Wd, 2)                               # host tensors
+
+
+def test_attn_case_and_decoder_wrappers_reject_wrong_shapes():
+    import torch
+    X = _t(4, 256)
+    with pytest.raises(ValueError, match="Wo"):
+        tpl.tp_attn_proj(X, _t(512, 256), _t(256, 128), 4, 2, 64, 2)        # Wo must be [256, 256]
+    with pytest.raises(ValueError, match="Wqkv"):
+        tpl.tp_attn_proj(X, _t(256, 256), _t(256, 256), 4, 2, 64, 2)       # Wqkv must be [512, 256]
+    with pytest.raises(ValueError, match="qkv_out"):
+        tpl.tp_attn_proj(X, _t(512, 256), _t(256, 256), 4, 2, 64, 2, qkv_out=_t(2, 4, 128))
+    with pytest.raises(TypeError, match="Bt"):
+        tpl.sharded_matmul(1, _t(16, 64), _t(32, 64, dtype=torch.float32), 2)
+    with pytest.raises(ValueError, match="out"):
+        tpl.sharded_matmul(3, _t(16, 64), _t(32, 64), 2, mode=tpl.REDUCE_SCATTER, out=_t(16, 32))
+    W = {"Wqkv": _t(512, 256), "Wo": _t(256, 256), "Wg": _t(512, 256), "Wu": _t(512, 256), "Wd": _t(256, 512)}
+    bad = dict(W, Wd=_t(512, 256))
+    with pytest.raises(ValueError, match="Wd"):
+        tpl.tp_decoder_stack(X, [W, bad], 4, 2, 64, 2)
+    with pytest.raises(ValueError, match="out"):
+        tpl.tp_decoder_layer(X, W, 4, 2, 64, 2, out=_t(4, 128))
+
+
+def test_static_scratch_limit_uses_the_calls_own_plan_and_dtype_comes_first():
+    """tpl_tp_mlp_forward_static_ws: the Llama-3.1-70B-shaped MLP (D 8192,
+    F 28672, tp 8) fits the static scratch up to B = 32 and not at B = 64;
+    the size check runs before any device is touched, after the dtype check."""
+    s = ctypes.c_void_p(0)
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(6)]
+    D, F, tp = 8192, 28672, 8
+    # without partials, then with: both plans exceed 32 MiB at B = 64
+    for part in (NULL, p[5]):
+        st = lib.tpl_tp_mlp_forward_static_ws(p[0], p[1], p[2], p[3], p[4], part, 64, D, F, tp, tpl.BF16,
+                                              tpl.BF16, s)
+        assert tpl.STATUS[st] == "TPL_ERR_STATIC_LIMIT"
+    # an output type tp_mlp_forward rejects is reported as such, not as a size problem
+    st = lib.tpl_tp_mlp_forward_static_ws(p[0], p[1], p[2], p[3], p[4], NULL, 64, D, F, tp, tpl.F32, tpl.BF16, s)
+    assert tpl.STATUS[st] == "TPL_ERR_DTYPE"
+    # the plan for the call's own partials argument decides, not the larger of the two
+    assert lib.tpl_tp_mlp_forward_workspace(32, D, F, tp, tpl.BF16, ctypes.byref(ctypes.c_size_t())) == 0
+    n = ctypes.c_size_t(0)
+    lib.tpl_tp_mlp_forward_workspace(32, D, F, tp, tpl.BF16, ctypes.byref(n))
+    assert n.value <= tpl.STATIC_WS_BYTES
