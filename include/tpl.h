@@ -150,11 +150,16 @@ tpl_status tpl_tp_mlp_forward(const void* X, const void* Wg, const void* Wu, con
  * holds that array until the process exits.
  *   - The caller still owns and passes X, the weights, Y and the optional
  *     partials.  No device memory is allocated or freed by this call.
- *   - The problem's workspace (tp_mlp_forward_workspace) must fit in
- *     TPL_STATIC_WS_BYTES, else TPL_ERR_STATIC_LIMIT and nothing is launched.
- *     Decode-sized calls fit, e.g. D 1536, F 8960 (tp 2) up to B = 128 and
- *     D 8192, F 28672 (tp 8) up to B = 32; a 4096-token prefill of the latter
- *     (352 MiB of workspace) does not.
+ *   - The scratch this call needs (the workspace plan of tp_mlp_forward for
+ *     the partials argument given) must fit in TPL_STATIC_WS_BYTES, else
+ *     TPL_ERR_STATIC_LIMIT and nothing is launched.  Shape and dtype errors
+ *     are reported first, with the codes tp_mlp_forward gives.  Decode-sized
+ *     calls fit, e.g. D 1536, F 8960 (tp 2) up to B = 128 and D 8192,
+ *     F 28672 (tp 8) up to B = 32; B = 64 of the latter and a 4096-token
+ *     prefill (352 MiB of workspace) do not.
+ *   - The array used is the one of the host thread's current device, so the
+ *     current device must be the one that owns the stream and the tensors.
+ *     A stream of another device gives TPL_ERR_UNSUPPORTED.
  *   - All calls on a device share the one array, which keeps what the last
  *     call left in it (nothing in it needs to start at zero).  Calls whose
  *     kernels overlap on the GPU -- on different streams or from different

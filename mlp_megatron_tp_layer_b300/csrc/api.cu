@@ -251,6 +251,15 @@ size_t mlp_ws_bytes(int64_t B, int64_t D, int64_t F, int tp, int dt) {
     return std::max(plan_mlp(B, D, F, tp, dt, true).total, plan_mlp(B, D, F, tp, dt, false).total);
 }
 
+}  // namespace
+
+size_t mlp_plan_bytes(int64_t B, int64_t D, int64_t F, int tp, int dt, bool want_partials) {
+    return plan_mlp(B, D, F, tp, dt, want_partials).total;
+}
+bool mlp_out_dtype_ok(int dt, int out_dt) { return out_dtype_ok(dt, out_dt); }
+
+namespace {
+
 tpl_status check_mlp_shape(int64_t B, int64_t D, int64_t F, int tp, int dt) {
     if (dt != TPL_F32 && dt != TPL_BF16) return TPL_ERR_DTYPE;
     if (B <= 0 || D <= 0 || F <= 0 || tp <= 0) return TPL_ERR_SHAPE;
@@ -468,6 +477,7 @@ extern "C" tpl_status tpl_device_status(unsigned int* flags, void* stream) {
 
 extern "C" tpl_status tpl_shard_reduce(const float* partials, void* out, int64_t rows, int64_t cols, int tp,
                                        int mode, int out_dtype, void* stream) {
+    TPL_NVTX_RANGE("tpl_shard_reduce");
     if (!partials || !out) return TPL_ERR_NULL;
     if (out_dtype != TPL_F32 && out_dtype != TPL_BF16) return TPL_ERR_DTYPE;
     if (rows <= 0 || cols <= 0 || tp <= 0) return TPL_ERR_SHAPE;
@@ -497,6 +507,7 @@ extern "C" tpl_status tpl_tp_mlp_forward_workspace(int64_t B, int64_t D, int64_t
 extern "C" tpl_status tpl_tp_mlp_forward(const void* X, const void* Wg, const void* Wu, const void* Wd, void* Y,
                                          float* partials, int64_t B, int64_t D, int64_t F, int tp, int dtype,
                                          int out_dtype, void* ws, size_t ws_bytes, void* stream) {
+    TPL_NVTX_RANGE("tpl_tp_mlp_forward");
     if (!X || !Wg || !Wu || !Wd || !Y) return TPL_ERR_NULL;
     tpl_status s = check_mlp_shape(B, D, F, tp, dtype);
     if (s != TPL_OK) return s;
@@ -531,6 +542,7 @@ extern "C" tpl_status tpl_tp_attn_proj_workspace(int64_t B, int64_t D, int n_q, 
 extern "C" tpl_status tpl_tp_attn_proj(const void* X, const void* Wqkv, const void* Wo, void* qkv_out, void* Y,
                                        float* partials, int64_t B, int64_t D, int n_q, int n_kv, int head_dim,
                                        int tp, int dtype, int out_dtype, void* ws, size_t ws_bytes, void* stream) {
+    TPL_NVTX_RANGE("tpl_tp_attn_proj");
     if (!X || !Wqkv || !Wo || !Y) return TPL_ERR_NULL;
     tpl_status s = check_attn_shape(B, D, n_q, n_kv, head_dim, tp, dtype);
     if (s != TPL_OK) return s;
@@ -617,6 +629,7 @@ extern "C" tpl_status tpl_sharded_matmul_workspace(int case_id, int mode, int64_
 extern "C" tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, const void* A, const void* Bt, void* C,
                                          float* partials, int64_t I, int64_t J, int64_t K, int X, int dtype,
                                          int out_dtype, void* ws, size_t ws_bytes, void* stream) {
+    TPL_NVTX_RANGE("tpl_sharded_matmul");
     if (!A || !Bt || !C) return TPL_ERR_NULL;
     tpl_status s = check_case(case_id, mode, gather, I, J, K, X, dtype);
     if (s != TPL_OK) return s;
@@ -696,6 +709,7 @@ extern "C" tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void
                                               const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,
                                               int n_q, int n_kv, int head_dim, int tp, void* ws, size_t ws_bytes,
                                               int path, int block, void* stream) {
+    TPL_NVTX_RANGE("tpl_tp_decoder_stack_ex");
     if (!Wqkv || !Wo || !Wg || !Wu || !Wd || !ws) return TPL_ERR_NULL;
     if (path != TPL_PATH_AUTO && path != TPL_PATH_UNFUSED && path != TPL_PATH_FUSED) return TPL_ERR_UNSUPPORTED;
     if (block != TPL_BLOCK_SERIAL && block != TPL_BLOCK_PARALLEL) return TPL_ERR_UNSUPPORTED;
@@ -801,6 +815,7 @@ bool al8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 extern "C" tpl_status tpl_quantize_w8(const void* W, int64_t rows, int64_t cols, int groups, int8_t* Q,
                                       float* scale, void* stream) {
+    TPL_NVTX_RANGE("tpl_quantize_w8");
     if (!W || !Q || !scale) return TPL_ERR_NULL;
     if (rows <= 0 || cols <= 0 || groups <= 0 || cols % groups != 0) return TPL_ERR_SHAPE;
     if ((cols / groups) % 8 != 0) return TPL_ERR_ALIGN;
@@ -825,6 +840,7 @@ extern "C" tpl_status tpl_tp_mlp_forward_w8(const void* X, const int8_t* Qg, con
                                             const float* su, const int8_t* Qd, const float* sd, void* Y,
                                             float* partials, int64_t B, int64_t D, int64_t F, int tp,
                                             int out_dtype, void* ws, size_t ws_bytes, void* stream) {
+    TPL_NVTX_RANGE("tpl_tp_mlp_forward_w8");
     if (!X || !Qg || !sg || !Qu || !su || !Qd || !sd || !Y) return TPL_ERR_NULL;
     tpl_status s = check_w8_shape(B, D, F, tp);
     if (s != TPL_OK) return s;
@@ -915,6 +931,7 @@ extern "C" tpl_status tpl_vocab_parallel_topk(const void* X, const void* W, int6
                                               int tp, int k, int dtype, int32_t* top_idx, float* top_val,
                                               int32_t* shard_idx, float* shard_val, void* ws, size_t ws_bytes,
                                               void* stream) {
+    TPL_NVTX_RANGE("tpl_vocab_parallel_topk");
     if (!X || !W || !top_idx) return TPL_ERR_NULL;
     tpl_status s = check_vocab_shape(B, V, tp, k);
     if (s != TPL_OK) return s;

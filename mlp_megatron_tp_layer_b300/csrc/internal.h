@@ -6,9 +6,22 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/tpl.h"
 
 namespace tpl {
+
+// NVTX range around one call of the C ABI: a profiler that records NVTX (nsys,
+// ncu --nvtx) shows each entry point by name around the kernels it launched.
+// Without a tool attached the push/pop calls do nothing.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define TPL_NVTX_RANGE(name) ::tpl::NvtxRange tpl_nvtx_range_(name)
 
 // ---------------------------------------------------------------- epilogues
 // How a GEMM-like kernel writes the value v computed for (token t, feature f).
@@ -66,6 +79,12 @@ struct DeviceCtx {
     unsigned int* err_word = nullptr;   // device address of the sticky error word
 };
 const DeviceCtx* device_ctx();          // nullptr if no CUDA device is usable
+
+// Workspace of one tp_mlp_forward call: the plan for the partials argument
+// actually given (null or not), as that call checks it.
+size_t mlp_plan_bytes(int64_t B, int64_t D, int64_t F, int tp, int dt, bool want_partials);
+// Whether out_dt is an output type tp_mlp_forward accepts for inputs of type dt.
+bool mlp_out_dtype_ok(int dt, int out_dt);
 
 // ------------------------------------------------------ CUDA-core kernels
 // rows of W (N rows, length K, pitch ldw) dotted with nb tokens of X (pitch ldx);

@@ -38,11 +38,21 @@ void* static_ws_address() {
 extern "C" tpl_status tpl_tp_mlp_forward_static_ws(const void* X, const void* Wg, const void* Wu, const void* Wd,
                                                    void* Y, float* partials, int64_t B, int64_t D, int64_t F,
                                                    int tp, int dtype, int out_dtype, void* stream) {
+    TPL_NVTX_RANGE("tpl_tp_mlp_forward_static_ws");
     if (!X || !Wg || !Wu || !Wd || !Y) return TPL_ERR_NULL;
-    size_t need = 0;
-    const tpl_status s = tpl_tp_mlp_forward_workspace(B, D, F, tp, dtype, &need);
+    size_t any = 0;
+    const tpl_status s = tpl_tp_mlp_forward_workspace(B, D, F, tp, dtype, &any);   // shape and dtype checks
     if (s != TPL_OK) return s;
-    if (need > (size_t)TPL_STATIC_WS_BYTES) return TPL_ERR_STATIC_LIMIT;
+    if (!tpl::mlp_out_dtype_ok(dtype, out_dtype)) return TPL_ERR_DTYPE;
+    // the scratch this call needs: the plan for the partials argument given
+    if (tpl::mlp_plan_bytes(B, D, F, tp, dtype, partials != nullptr) > (size_t)TPL_STATIC_WS_BYTES)
+        return TPL_ERR_STATIC_LIMIT;
+    // the array used is the current device's, so the stream must be that
+    // device's too (the tensors are the caller's to place on it)
+    int cur = -1, sdev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return TPL_ERR_CUDA;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return TPL_ERR_CUDA;
+    if (sdev != cur) return TPL_ERR_UNSUPPORTED;
     void* ws = static_ws_address();
     if (!ws) return TPL_ERR_CUDA;
     // Nothing in the MLP's scratch has to start at zero: every element of the

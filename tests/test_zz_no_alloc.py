@@ -69,6 +69,29 @@ def test_static_scratch_matches_workspace_entry_point(B):
         assert_close(Yb, to_np(ref_b), rel=BF16_REL, bf16_out=True, what=f"call {call}: Y bf16")
 
 
+def test_static_scratch_llama_shaped_mlp_at_its_largest_batch():
+    """The Llama-3.1-70B-shaped MLP (D 8192, F 28672, tp 8) at B = 32, the
+    largest decode batch whose scratch fits the static array, against the
+    workspace entry point, two calls in a row."""
+    B, D, F, tp = 32, 8192, 28672, 8
+    assert tpl.mlp_workspace_bytes(B, D, F, tp) <= tpl.STATIC_WS_BYTES
+    Wg = si.normal((F, D), 0.02, 12, "na.Wg70", device="cuda")
+    Wu = si.normal((F, D), 0.02, 12, "na.Wu70", device="cuda")
+    Wd = si.normal((D, F), 0.02, 12, "na.Wd70", device="cuda")
+    for call in range(2):
+        X = si.normal((B, D), 1.0, 200 + call, "na.X70", device="cuda")
+        ref32, ref_p = tpl.tp_mlp_forward(X, Wg, Wu, Wd, tp, out_dtype=torch.float32, partials=True)
+        Y32 = torch.full((B, D), float("nan"), dtype=torch.float32, device="cuda")
+        P = torch.full((tp, B, D), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call_static(X, Wg, Wu, Wd, tp, Y32, P) == 0
+        torch.cuda.synchronize()
+        assert_close(Y32, to_np(ref32), rel=BF16_REL, what=f"call {call}: Y fp32")
+        for s in (0, tp - 1):
+            assert_close(P[s], to_np(ref_p[s]), rel=BF16_REL, what=f"call {call}: P_{s}")
+    del Wg, Wu, Wd
+    torch.cuda.empty_cache()
+
+
 def test_static_scratch_rejects_problems_beyond_its_size():
     # Llama-3.1-70B-shaped prefill MLP: 352 MiB of workspace > 32 MiB
     B, D, F, tp = 4096, 8192, 28672, 8
