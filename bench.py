@@ -233,21 +233,59 @@ def cpu_baseline(layers_dev, budget_s):
         return n, time.perf_counter() - t0
 
     n, dt = timed(budget_s)
-    single = None
+    single, why = None, None
     try:
-        # the same oracle on one host thread (a quarter of the budget)
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1, user_api="blas"):
-            n1, dt1 = timed(budget_s / 4)
-        single = n1 * QWEN_LAYER_BYTES / dt1 / 1e9
-    except Exception:  # noqa: BLE001
-        pass
+        single = oracle_one_thread(W, xs, budget_s / 4)
+    except Exception as e:  # noqa: BLE001
+        why = f"{type(e).__name__}: {e}"[:300]
     del np
-    return {"value": n * QWEN_LAYER_BYTES / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "single_thread_value": single,
-            "sample": f"{n // len(QW['batches'])} passes of one Qwen-shaped TP=2 layer over B in "
-                      f"{list(QW['batches'])} (numpy float64), {dt:.1f} s; then one thread for a quarter "
-                      f"of that budget"}
+    out = {"value": n * QWEN_LAYER_BYTES / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "single_thread_value": single,
+           "sample": f"{n // len(QW['batches'])} passes of one Qwen-shaped TP=2 layer over B in "
+                     f"{list(QW['batches'])} (numpy float64), {dt:.1f} s; then the same in a child process "
+                     f"with every BLAS/OpenMP pool at one thread, for a quarter of that budget"}
+    if why:
+        out["single_thread_error"] = why
+    return out
+
+
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                  "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def oracle_one_thread(W, xs, budget_s):
+    """GB/s of the oracle decoding one Qwen-shaped layer at every batch size in
+    a child process whose thread pools are all limited to one thread by the
+    environment (set before numpy loads its BLAS); the arrays go by file."""
+    import numpy as np
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    try:
+        np.savez(path, **{f"W_{k}": v for k, v in W.items()}, **{f"x_{B}": v for B, v in xs.items()})
+        code = (
+            "import sys, time, numpy as np\n"
+            f"sys.path.insert(0, {ROOT!r})\n"
+            "from oracle import tp_layer as O\n"
+            "z = np.load(sys.argv[1])\n"
+            "W = {k[2:]: z[k] for k in z.files if k.startswith('W_')}\n"
+            "xs = [z[k] for k in z.files if k.startswith('x_')]\n"
+            f"n, t0 = 0, time.perf_counter()\n"
+            "while True:\n"
+            "    for x in xs:\n"
+            f"        O.decoder_layer(x, W, {QW['n_q']}, {QW['n_kv']}, {QW['head_dim']}, {QW['tp']})\n"
+            "        n += 1\n"
+            f"    if time.perf_counter() - t0 > {budget_s}:\n"
+            "        break\n"
+            "print(n, time.perf_counter() - t0)\n")
+        env = dict(os.environ, **{k: "1" for k in ONE_THREAD_ENV})
+        r = subprocess.run([sys.executable, "-c", code, path], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 4 + 120)
+        if r.returncode != 0:
+            raise RuntimeError(r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}")
+        n, dt = r.stdout.split()
+        return int(n) * QWEN_LAYER_BYTES / float(dt) / 1e9
+    finally:
+        os.unlink(path)
 
 
 def run_reference(args, rank, world):

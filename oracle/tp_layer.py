@@ -16,7 +16,7 @@ Sources (pages of the reference material, by title and section):
         parallelism: ColumnParallelLinear stores its weight as
         [output_size_per_partition, input_size] and applies F.linear.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * SwiGLU is silu(gate) * up with silu(z) = z / (1 + exp(-z))  ([L4] S4.1 only
     says "element-wise").
   * Weights are stored [out, in] ([V4] S2.1); shard s of a split dimension of

@@ -12,7 +12,7 @@ the scores of V/n vocabulary entries, and the full logits are normally
 all-gathered.  When only the next token is needed, each device can first take
 its own maximum (or top-k) and only those candidates are exchanged.
 
-Readings where the section is silent (each also listed in the design doc):
+Readings where the section is silent:
   * The lm_head weight is stored [V, D] (one row per vocabulary entry, the
     [out, in] layout of the other projections); shard s owns the contiguous
     rows [s V/tp, (s+1) V/tp), so V must divide by tp.

@@ -11,7 +11,7 @@ quantised, which saves the time spent reading them (PaLM 540B decode at B = 64:
 28.5 ms per token with int8 weights against 36.9 ms in bf16); S6.2: the cheapest
 configurations are the ones whose weights take half the bytes.
 
-Readings where the section is silent (each also listed in the design doc):
+Readings where the section is silent:
   * Symmetric per-row quantisation: a row of W (one output feature) is split
     into `groups` contiguous column groups -- one per tensor-parallel shard for
     a row-parallel weight, so every device quantises only what it holds -- and

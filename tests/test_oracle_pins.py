@@ -380,6 +380,61 @@ def test_decoder_layer_zero_output_projections_is_identity():
     assert np.allclose(y, O.bf16_round(x + a), rtol=0, atol=2 ** -7 * np.abs(x + a).max())
 
 
+def _serial_layer_with_silenced_attention():
+    """[L4] S5.5 block formula, serial form, attention output projection zero:
+    h = x exactly, so y = bf16(x + MLP(RMSNorm(x))), with the MLP written out
+    here in plain loops (no shards; SiLU from math.exp; H rounded to bf16)."""
+    r = rng(17)
+    D, F, n_q, n_kv, hd = 12, 20, 4, 2, 3
+    x = O.bf16_round(r.standard_normal((2, D)) * 1.5)
+    W = dict(Wqkv=r.standard_normal(((n_q + 2 * n_kv) * hd, D)), Wo=np.zeros((D, n_q * hd)),
+             Wg=r.standard_normal((F, D)) / 3, Wu=r.standard_normal((F, D)) / 3, Wd=r.standard_normal((D, F)) / 4)
+    ref = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        ms = sum(float(v) * float(v) for v in x[t]) / D
+        inv = 1.0 / math.sqrt(ms + O.RMS_EPS)
+        xn = [float(v) * inv for v in x[t]]
+        H = []
+        for f in range(F):
+            g = sum(W["Wg"][f, d] * xn[d] for d in range(D))
+            u = sum(W["Wu"][f, d] * xn[d] for d in range(D))
+            H.append(float(O.bf16_round(np.array(g / (1.0 + math.exp(-g)) * u))))
+        for d in range(D):
+            ref[t, d] = x[t, d] + sum(W["Wd"][d, f] * H[f] for f in range(F))
+    ref = O.bf16_round(ref)
+    return x, W, ref, (n_q, n_kv, hd)
+
+
+def _serial_mlp_pin_holds(x, W, ref, dims, tp):
+    y = O.decoder_layer(x, W, *dims, tp=tp)
+    # one bf16 rounding of nearby values (sum order only) may differ by an ulp
+    return bool(np.all(np.abs(y - ref) <= 2 ** -7 * np.abs(ref) + 1e-12))
+
+
+def test_serial_layer_mlp_branch_pin():
+    x, W, ref, dims = _serial_layer_with_silenced_attention()
+    for tp in (1, 2, 4):
+        assert _serial_mlp_pin_holds(x, W, ref, dims, tp), tp
+
+
+def test_serial_layer_mlp_branch_pin_catches_planted_mistakes(monkeypatch):
+    x, W, ref, dims = _serial_layer_with_silenced_attention()
+    real_norm, real_silu, real_hidden = O.rmsnorm, O.silu, O.mlp_hidden_shard
+    monkeypatch.setattr(O, "rmsnorm", lambda v, eps=O.RMS_EPS: np.asarray(v, dtype=np.float64))  # norm dropped
+    assert not _serial_mlp_pin_holds(x, W, ref, dims, 2)
+    monkeypatch.setattr(O, "rmsnorm", real_norm)
+    monkeypatch.setattr(O, "silu", lambda z: np.asarray(z, dtype=np.float64))                     # SiLU dropped
+    assert not _serial_mlp_pin_holds(x, W, ref, dims, 2)
+    monkeypatch.setattr(O, "silu", real_silu)
+
+    def swapped(X, Wg, Wu, tp, s, bf16=True):                                                  # gate <-> up
+        return real_hidden(X, Wu, Wg, tp, s, bf16)
+    monkeypatch.setattr(O, "mlp_hidden_shard", swapped)
+    assert not _serial_mlp_pin_holds(x, W, ref, dims, 2)
+    monkeypatch.setattr(O, "mlp_hidden_shard", real_hidden)
+    assert _serial_mlp_pin_holds(x, W, ref, dims, 2)
+
+
 def test_parallel_block_reduces_to_its_sublayers():
     """[L4] S5.5 parallel block: silencing one sublayer's output projection leaves
     x plus the other sublayer on RMSNorm(x), each computed here without shards."""
