@@ -219,6 +219,61 @@ __global__ void reduce_kernel(const ReduceArgs a) {
     }
 }
 
+// The plain shard sum (one split per shard, no gate/up pair, no per-shard
+// copies, no RMSNorm): y = residual + P_0 + P_1 + ... + P_{TP-1}, added in
+// ascending shard order like reduce_kernel, four consecutive elements per
+// item and two items per thread, with all 2 TP partial loads issued before
+// the first add (streaming loads: every partial is read once), so enough
+// bytes are in flight to keep HBM busy.
+template <int TP>
+__global__ void __launch_bounds__(256) shard_sum_kernel(const ReduceArgs a) {
+    const int64_t n4 = a.rows * a.cols / 4;
+    const float4* ws = reinterpret_cast<const float4*>(a.ws);
+    const int64_t cw = a.mode == TPL_ALLREDUCE ? a.cols : a.cols / TP;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x * 2;
+    for (int64_t j0 = (int64_t)blockIdx.x * blockDim.x * 2 + threadIdx.x; j0 < n4; j0 += step) {
+        float4 v[2][TP];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t j = j0 + (int64_t)u * blockDim.x;
+            if (j < n4) {
+#pragma unroll
+                for (int s = 0; s < TP; ++s) v[u][s] = __ldcs(ws + (int64_t)s * n4 + j);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t j = j0 + (int64_t)u * blockDim.x;
+            if (j >= n4) continue;
+            float4 y = v[u][0];
+#pragma unroll
+            for (int s = 1; s < TP; ++s) { y.x += v[u][s].x; y.y += v[u][s].y; y.z += v[u][s].z; y.w += v[u][s].w; }
+            const int64_t i = j * 4;
+            if (a.residual) {
+                const uint2 r = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.residual) + i);
+                y.x += __uint_as_float(r.x << 16); y.y += __uint_as_float(r.x & 0xFFFF0000u);
+                y.z += __uint_as_float(r.y << 16); y.w += __uint_as_float(r.y & 0xFFFF0000u);
+            }
+            // four consecutive elements lie in one row and, for reduce-scatter,
+            // in one column block (cw is a multiple of 4)
+            int64_t o = i;
+            if (a.mode != TPL_ALLREDUCE) {
+                const int64_t row = i / a.cols, c = i - row * a.cols, sb = c / cw;
+                o = sb * a.rows * cw + row * cw + (c - sb * cw);
+            }
+            if (a.y_bf16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
+                uint2 w;
+                w.x = *reinterpret_cast<const uint32_t*>(&lo);
+                w.y = *reinterpret_cast<const uint32_t*>(&hi);
+                __stcs(reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.y) + o), w);
+            } else {
+                __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + o), y);
+            }
+        }
+    }
+}
+
 constexpr int kNormThreads = kNormCols / 4;     // 4 columns per thread
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -317,7 +372,22 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t st) {
     }
     const int64_t n4 = (a.rows * a.cols + 3) / 4;
     const DeviceCtx* ctx = device_ctx();
-    const int64_t max_blocks = (int64_t)(ctx ? ctx->num_sms : 148) * 16;
+    const int64_t sms = ctx ? ctx->num_sms : 148;
+    if (a.sub == 1 && !a.ws_up && !a.shard_out && a.tp >= 1 && a.tp <= 8 && a.cols % 4 == 0) {
+        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((n4 + 511) / 512, sms * 8));
+        switch (a.tp) {
+        case 1: shard_sum_kernel<1><<<blocks, 256, 0, st>>>(a); break;
+        case 2: shard_sum_kernel<2><<<blocks, 256, 0, st>>>(a); break;
+        case 3: shard_sum_kernel<3><<<blocks, 256, 0, st>>>(a); break;
+        case 4: shard_sum_kernel<4><<<blocks, 256, 0, st>>>(a); break;
+        case 5: shard_sum_kernel<5><<<blocks, 256, 0, st>>>(a); break;
+        case 6: shard_sum_kernel<6><<<blocks, 256, 0, st>>>(a); break;
+        case 7: shard_sum_kernel<7><<<blocks, 256, 0, st>>>(a); break;
+        default: shard_sum_kernel<8><<<blocks, 256, 0, st>>>(a); break;
+        }
+        return cudaGetLastError();
+    }
+    const int64_t max_blocks = sms * 16;
     const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((n4 + 127) / 128, max_blocks));
     reduce_kernel<<<blocks, 128, 0, st>>>(a);
     return cudaGetLastError();
