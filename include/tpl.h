@@ -235,10 +235,11 @@ tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, const void* A, 
  * a whole decode step.
  *
  * Two implementations compute it.  FUSED (B <= 128 tokens; D, F and
- * n_q head_dim multiples of 64): one persistent cooperative launch per up to
+ * head_dim multiples of 64): one persistent cooperative launch per up to
  * 32 layers streams every weight once through tensor-core GEMMs with the
- * weights as the M operand; split-K partial tiles are added by the last CTA
- * to finish each tile, in k (shard) order.  UNFUSED: one launch per
+ * weights as the M operand; split-K partial tiles are added, in k (shard)
+ * order, by the CTAs that computed them, and each projection starts on the
+ * tiles whose inputs are final (per-tile readiness, no grid-wide barrier).  UNFUSED: one launch per
  * projection and per shard reduction.  The two add partial sums in
  * different orders, so they agree to rounding, not bit for bit; each is
  * deterministic.  tpl_tp_decoder_stack / _layer take FUSED where it applies.
@@ -374,6 +375,31 @@ tpl_status tpl_vocab_parallel_topk(const void* X, const void* W, int64_t B, int6
 tpl_status tpl_profile_enable(int max_launches);
 int tpl_profile_count(void);
 tpl_status tpl_profile_read(int i, char* tag, size_t tag_len, float* ms);
+
+/* --------------------------------------------------------------------------
+ * Test hook for the failure path of the fused decode stack (off by default).
+ * Not a step of the method: the pages name the failure it stands in for -- a
+ * collective that never completes because one rank never arrives (the NCCL
+ * hang and timeout modes of the TP serving pages) -- and this makes that
+ * happen on one GPU without a fault.
+ *
+ * Every wait of the fused stack (between CTAs: tile tickets, tile readiness,
+ * phase completion; inside a CTA: the mbarriers of its pipeline) gives up
+ * after a time limit, raises the launch's abort flag so that every CTA stops
+ * waiting, drains its copies and MMAs in flight, frees its tensor memory and
+ * returns; the sticky device error word then holds TPL_DEVERR_TIMEOUT
+ * (tpl_device_status).  tpl_test_fused_fault(cta, phase, wait_limit_ns)
+ * applies to the fused-stack launches issued after it:
+ *   - cta >= 0: CTA `cta` does not count its first unit of phase `phase`
+ *     (>= 1; phase 4 l + 1 + j is projection j of layer l of the launch, in
+ *     the block's phase order) on its tile's ticket, so the tile's finalize
+ *     waits until the limit passes.  cta < 0 turns the omission off.
+ *   - wait_limit_ns > 0 sets the limit (10 us .. 2 s); <= 0 restores 2 s.
+ * After such a launch the workspace needs nothing: the next launch starts
+ * from zeroed counters and rewrites every buffer before reading it.
+ * Returns TPL_ERR_UNSUPPORTED for arguments out of range.
+ * ------------------------------------------------------------------------ */
+tpl_status tpl_test_fused_fault(int cta, int phase, int64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

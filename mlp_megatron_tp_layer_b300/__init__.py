@@ -50,6 +50,7 @@ _SIGS = {
     "tpl_profile_enable": (_i32, [_i32]),
     "tpl_profile_count": (_i32, []),
     "tpl_profile_read": (_i32, [_i32, ctypes.c_char_p, _sz, ctypes.POINTER(ctypes.c_float)]),
+    "tpl_test_fused_fault": (_i32, [_i32, _i32, _i64]),
     "tpl_tp_decoder_workspace": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tpl_tp_decoder_stack_path": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
@@ -412,6 +413,13 @@ def tp_decoder_layer(x, W, n_q, n_kv, head_dim, tp, out=None, ws=None, stream=No
                                     _p(W["Wd"]), B, D, F, n_q, n_kv, head_dim, tp, _p(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "tpl_tp_decoder_layer")
     return out
+
+
+def test_fused_fault(cta: int = -1, phase: int = 1, wait_limit_ns: int = 0):
+    """Test hook (tpl_test_fused_fault): make CTA `cta` of the next fused-stack
+    launches leave out its first ticket arrival of `phase`, with every wait
+    limited to wait_limit_ns; test_fused_fault() restores the defaults."""
+    _check(lib.tpl_test_fused_fault(cta, phase, wait_limit_ns), "tpl_test_fused_fault")
 
 
 def profile_enable(max_launches: int = 4096):

@@ -747,6 +747,14 @@ extern "C" tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void
     return TPL_OK;
 }
 
+extern "C" tpl_status tpl_test_fused_fault(int cta, int phase, int64_t wait_limit_ns) {
+    if (wait_limit_ns > 2000000000LL) return TPL_ERR_UNSUPPORTED;
+    if (wait_limit_ns > 0 && wait_limit_ns < 10000) return TPL_ERR_UNSUPPORTED;
+    if (cta >= kFusedGridCap || (cta >= 0 && phase < 1)) return TPL_ERR_UNSUPPORTED;
+    fused_test_fault(cta < 0 ? -1 : cta, cta < 0 ? -1 : phase, wait_limit_ns);
+    return TPL_OK;
+}
+
 extern "C" tpl_status tpl_tp_decoder_stack_path(const void* x, void* y, const void* const* Wqkv,
                                                 const void* const* Wo, const void* const* Wg, const void* const* Wu,
                                                 const void* const* Wd, int n_layers, int64_t B, int64_t D, int64_t F,

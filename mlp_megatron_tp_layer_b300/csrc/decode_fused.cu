@@ -22,14 +22,20 @@
 // phase's epilogue.  The sum is therefore the same whatever order the CTAs
 // ran in.
 //
-// Phases are separated by a grid barrier: one counter in global memory that
-// every CTA increments when it has finished a phase, and only after the
-// barrier of that phase has passed, so that it reaching G (k+1) means phases
-// 0..k are complete everywhere.  The launch is cooperative, so every CTA is
-// resident and these waits (all bounded in time) can be met.  Weight tiles do
-// not depend on the activations, so the weight producer keeps loading the
-// next phase's weights into the shared-memory ring while the barrier is
-// pending; only the activation loads wait for it.
+// There is no grid-wide barrier between phases.  Each output tile of a phase
+// has a ready counter (tokens finalized, monotone over the layers of the
+// launch); a unit's activation loads wait only for the tiles of the previous
+// phase that its k-blocks read, so a phase starts wherever its inputs are
+// final.  Each phase also has a done counter (tokens finalized over all its
+// tiles), and a phase finalizes no tile before the previous finalizing phase
+// is done.  By induction every earlier phase is then complete, which is what
+// makes it safe to overwrite the buffers the layers share: a phase's partial
+// slots (one region per projection kind), its output tile, and the RMSNorm
+// tile sums are rewritten only after every reader of the previous contents
+// has finished.  The launch is cooperative, so every CTA is resident and these
+// waits (all bounded in time) can be met.  Weight tiles do not depend on the
+// activations, so the weight producer keeps loading the next phases' weights
+// into the shared-memory ring while their inputs are pending.
 //
 // RMSNorm: the producer of a residual-stream value also writes, per 128-column
 // tile and token, the sum of squares of the rounded values; the consumer's
@@ -44,6 +50,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <type_traits>
 
@@ -55,6 +62,10 @@ namespace tpl {
 namespace {
 
 constexpr int kFThreads = 224;
+#ifndef TPL_FUSED_PREFETCH
+#define TPL_FUSED_PREFETCH 0
+#endif
+constexpr int kFusedPrefetch = TPL_FUSED_PREFETCH;   // weight tiles prefetched to L2 ahead of the ring
 constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
@@ -72,18 +83,21 @@ struct FusedParams {
     int B, D, F, L, G;
     int parallel;              // 1: parallel block ([L4] S5.5), 0: serial pre-norm block
     int n_qkv, ko;             // packed QKV rows, o_proj input width n_q hd
-    int max_mt;                // ticket row length
+    int max_mt;                // length of a ticket / ready row
     float eps;
     QkvMap qkv;                // packed-QKV scatter (qkv_out = shard blocks, o_out = O)
     const __nv_bfloat16* x_in;
     __nv_bfloat16 *y_out, *R0, *R1, *O, *h, *H;
     float* slots_y;            // [ceil(D/128)][B] sums of squares of the layer input / output
     float* slots_h;            // [ceil(D/128)][B] sums of squares of h
-    float* part;               // partial tiles, [G + max_mt][2][NP][128] fp32
-    unsigned* tickets;         // [4][max_mt]
-    unsigned* bar;             // grid barrier counter (zero at launch)
+    float* part;               // partial tiles, [4 kinds][G + max_mt][2][NP][128] fp32
+    unsigned* tickets;         // [4][max_mt] units arrived per tile (monotone over the layers)
+    unsigned* ready;           // [4][max_mt] tokens finalized per output tile (monotone)
+    unsigned* done;            // [1 + 4 L] tokens finalized per phase (phase 0: input tile sums)
     int* gabort;               // grid abort flag (zero at launch)
     unsigned* err;
+    uint64_t wait_ns;          // time limit of every wait between CTAs and roles
+    int skip_cta, skip_phase;  // test hook: that CTA does not count its first unit of that phase (-1: off)
 };
 
 template <int NP>
@@ -94,7 +108,7 @@ struct FCfg {
     static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int CTRL = 1024;                            // mbarriers and flags
-    static constexpr int EPI = 128 * 4 + (2 * kFusedGridCap + 8) * 4;   // RMSNorm scales, two segment lists
+    static constexpr int EPI = (2 * kFusedGridCap + 8) * 4;     // two segment lists and their counts
     static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI;
     static constexpr int PART_FLOATS = 2 * NP * 128;             // one partial slot
     static constexpr int CH = NP >= 32 ? 32 : 16;                // TMEM columns per load
@@ -105,9 +119,9 @@ struct FCfg {
 
 struct Phase {
     int kind, layer, m_tiles, nkb, M;
-    int stage;                 // grid-barrier stage the phase's activations wait for
-    bool last_of_stage;        // the CTA signals the stage after this phase
-    int region;                // partial-slot region (two phases of one stage must not share one)
+    int prev_fin;              // phase whose completion this phase's finalize waits for (-1: none)
+    int src_kind;              // kind whose output tiles the activation loads wait for (-1: launch input)
+    unsigned src_target;       // ready count of such a tile once this layer's input is final
     int64_t total;
     const CUtensorMap* wa;
     const CUtensorMap* wb;
@@ -115,42 +129,47 @@ struct Phase {
 };
 
 // Phase k >= 1 of the launch: layer (k-1)/4, projection (k-1)%4.  Serial
-// block: QKV, o_proj, gate/up, down, each its own stage.  Parallel block: QKV
-// and gate/up (both on RMSNorm(x)) form one stage, o_proj and down (their
-// partials summed together into y) the next.
+// block: QKV, o_proj, gate/up, down.  Parallel block: QKV and gate/up (both
+// on RMSNorm(x)), then o_proj and down, whose partials are summed together
+// into y by down's finalize (o_proj finalizes nothing of its own).
 __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams& p, int k) {
     Phase ph;
     ph.layer = (k - 1) >> 2;
     const int pos = (k - 1) & 3;
     const int l = ph.layer;
+    const unsigned B = (unsigned)p.B;
     if (p.parallel) {
         constexpr int order[4] = {K_QKV, K_GATEUP, K_OPROJ, K_DOWN};
         ph.kind = order[pos];
-        ph.stage = 1 + 2 * l + (pos >> 1);
-        ph.last_of_stage = (pos & 1) != 0;
-        ph.region = (ph.kind == K_QKV || ph.kind == K_OPROJ) ? 1 : 0;
+        ph.prev_fin = ph.kind == K_OPROJ ? -1 : (ph.kind == K_DOWN ? k - 2 : k - 1);
     } else {
         ph.kind = pos;
-        ph.stage = k;
-        ph.last_of_stage = true;
-        ph.region = 0;
+        ph.prev_fin = k - 1;
     }
+    // the layer input y(l-1) is tile-ready once down of layer l-1 finalized it
+    const bool from_x = ph.kind == K_QKV || (p.parallel && ph.kind == K_GATEUP);
     int K, wa, wb = -1;
     switch (ph.kind) {
     case K_QKV:
         ph.M = p.n_qkv; K = p.D; wa = W_QKV;
-        ph.act = &mp.act[l == 0 ? A_X : (((l - 1) & 1) ? A_R1 : A_R0)];
         break;
     case K_OPROJ:
         ph.M = p.D; K = p.ko; wa = W_O; ph.act = &mp.act[A_O];
+        ph.src_kind = K_QKV; ph.src_target = B * (unsigned)(l + 1);
         break;
     case K_GATEUP:
         ph.M = p.F; K = p.D; wa = W_G; wb = W_U;
-        ph.act = p.parallel ? &mp.act[l == 0 ? A_X : (((l - 1) & 1) ? A_R1 : A_R0)] : &mp.act[A_H];
+        if (!p.parallel) { ph.act = &mp.act[A_H]; ph.src_kind = K_OPROJ; ph.src_target = B * (unsigned)(l + 1); }
         break;
     default:
         ph.M = p.D; K = p.F; wa = W_D; ph.act = &mp.act[A_HID];
+        ph.src_kind = K_GATEUP; ph.src_target = B * (unsigned)(l + 1);
         break;
+    }
+    if (from_x) {
+        ph.act = &mp.act[l == 0 ? A_X : (((l - 1) & 1) ? A_R1 : A_R0)];
+        ph.src_kind = l == 0 ? -1 : K_DOWN;
+        ph.src_target = B * (unsigned)l;
     }
     ph.wa = &mp.w[l][wa];
     ph.wb = wb < 0 ? nullptr : &mp.w[l][wb];
@@ -158,6 +177,28 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     ph.nkb = (K + 63) / 64;
     ph.total = (int64_t)ph.m_tiles * ph.nkb;
     return ph;
+}
+
+// Tokens a phase has finalized once it is complete (phase 0: the tile sums
+// of squares of the launch input, B per 128-column tile).
+__device__ __forceinline__ unsigned done_target(const FusedMaps& mp, const FusedParams& p, int k) {
+    if (k == 0) return (unsigned)((p.D + 127) / 128) * (unsigned)p.B;
+    return (unsigned)phase_of(mp, p, k).m_tiles * (unsigned)p.B;
+}
+
+// The output tile of phase ph.src_kind that k-block kb of ph's activations
+// lies in.  o_proj's input O is the context-1 attention output: column block
+// kb belongs to Q head h = 64 kb / hd, whose value is V of KV group
+// g = h / (n_q / n_kv), i.e. packed-QKV rows (n_q + n_kv + g) hd + (64 kb mod hd)
+// (a 64-wide block never straddles two heads: hd % 64 == 0).  Every other
+// input is the previous phase's output read in place: 128-wide tile kb / 2.
+__device__ __forceinline__ int src_tile(const FusedParams& p, const Phase& ph, int kb) {
+    if (ph.kind != K_OPROJ) return kb >> 1;
+    const int hd = p.qkv.head_dim;
+    const int col = kb * 64;
+    const int head = col / hd;
+    const int g = head / (p.qkv.n_q / p.qkv.n_kv);
+    return ((p.qkv.n_q + p.qkv.n_kv + g) * hd + (col - head * hd)) >> 7;
 }
 
 // The CTA owning flattened index a: the largest c with floor(c T / G) <= a.
@@ -233,7 +274,7 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 
 // Bounded wait until a counter in global memory reaches target (acquire).
 __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, volatile int* labort,
-                                       volatile int* gabort) {
+                                       volatile int* gabort, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
         unsigned v;
@@ -241,7 +282,49 @@ __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, vol
         if (v >= target) return true;
         if ((i & 15u) == 15u) {
             if (*labort || *gabort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
+        }
+        if (i > 64) __nanosleep(32);
+    }
+}
+
+// Release-publish two counter increments: every write this thread (and,
+// through a preceding barrier, its CTA) made is visible before either count.
+__device__ __forceinline__ void publish2(unsigned* a, unsigned* b, unsigned v) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(b), "r"(v) : "memory");
+}
+
+// Warp-collective: how many of the k-blocks kb, kb+1, .. < kb1 (at most 32)
+// lead with their source tiles final, waiting until at least one is.  Lane j
+// polls the ready counter of k-block kb+j (acquire); the count returned is
+// the same in every lane.  0: the wait gave up (time limit or abort).  Every
+// lane then fences the async proxy, so the TMA loads issued after the warp
+// barrier see the tiles' contents.
+__device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& ph, int kb, int kb1, int lane,
+                                         volatile int* labort, volatile int* gabort) {
+    const int want = min(kb1 - kb, 32);
+    const unsigned* ctr = lane < want ? p.ready + ph.src_kind * p.max_mt + src_tile(p, ph, kb + lane) : nullptr;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        bool r = true;
+        if (ctr) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+            r = v >= ph.src_target;
+        }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, r);
+        const int lead = __ffs(~m) == 0 ? 32 : __ffs(~m) - 1;     // leading ready k-blocks
+        const int n = min(want, lead);
+        if (n > 0) {
+            fence_proxy_async_global();
+            __syncwarp();
+            return n;
+        }
+        if ((i & 15u) == 15u) {
+            const bool stop = *labort || *gabort || globaltimer() - t0 > p.wait_ns;
+            if (__any_sync(0xFFFFFFFFu, stop)) return 0;
         }
         if (i > 64) __nanosleep(32);
     }
@@ -262,9 +345,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
     volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(ctrl + 1008);
-    float* scale = reinterpret_cast<float*>(ctrl + C::CTRL);    // [128] RMSNorm scales of the phase input
-    int* seg = reinterpret_cast<int*>(scale + 128);             // partial slots of the tile being finalized
+    int* seg = reinterpret_cast<int*>(ctrl + C::CTRL);          // partial slots of the tile being finalized
     int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
     volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, jseg, nseg2, jseg2]
 
@@ -285,7 +366,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         }
         mbar_init(smem_addr(drain), 1);
         *labort = 0;
-        *last_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -308,6 +388,17 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             TileCursor ld{};
+            // a second cursor runs kFusedPrefetch tiles ahead and brings those
+            // tiles into L2, so HBM keeps streaming while the ring is full
+            // (waiting for activations) and the ring's loads hit L2
+            TileCursor pf{};
+            bool pf_more = kFusedPrefetch > 0;
+            for (int i = 0; i < kFusedPrefetch && pf_more; ++i) {
+                const CUtensorMap* pm;
+                int px, py;
+                pf_more = pf.next(mp, p, G, cta, n_phases, pm, px, py);
+                if (pf_more) tma_prefetch_l2(pm, px, py);
+            }
             int stage = 0;
             uint32_t par = 0;
             int last_par[C::STAGES];           // parity of the latest copy issued into each stage, -1: none
@@ -316,10 +407,16 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             int x, y;
             bool ok = true;
             while (ok && ld.next(mp, p, G, cta, n_phases, map, x, y)) {
-                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort)) { ok = false; break; }
+                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
                 const uint32_t fb = smem_addr(&full_w[stage]);
                 mbar_expect_tx(fb, C::W_BYTES);
                 tma_load_hint(smem_addr(smem + stage * C::STAGE), map, fb, x, y, pol);
+                if (pf_more) {
+                    const CUtensorMap* pm;
+                    int px, py;
+                    pf_more = pf.next(mp, p, G, cta, n_phases, pm, px, py);
+                    if (pf_more) tma_prefetch_l2(pm, px, py);
+                }
                 last_par[stage] = (int)par;
                 if (++stage == C::STAGES) { stage = 0; par ^= 1; }
             }
@@ -336,55 +433,59 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         }
     } else if (warp == kWarpAct) {
         // ---------------------------------------------------- activation producer
-        // Fills the activation half of each stage once the phase's grid
-        // barrier has passed.  The second stage of a gate/up k-block reuses
-        // the first one's activations: its activation barrier still completes
-        // a phase (a plain arrive), so every barrier of the ring advances once
+        // Fills the activation half of each stage once the source tiles of its
+        // k-block are final (the whole warp polls their ready counters, lane 0
+        // issues the copies).  The second stage of a gate/up k-block reuses the
+        // first one's activations: its activation barrier still completes a
+        // phase (a plain arrive), so every barrier of the ring advances once
         // per round and the parities stay in step.
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_last();
-            int stage = 0;
-            uint32_t par = 0;
-            int last_par[C::STAGES];
-            for (int s = 0; s < C::STAGES; ++s) last_par[s] = -1;
-            bool ok = true;
-            for (int k = 1; k < n_phases && ok; ++k) {
-                const Phase ph = phase_of(mp, p, k);
-                const int halves = ph.kind == K_GATEUP ? 2 : 1;
-                Units u(ph, G, cta);
-                int mt, kb0, kb1;
-                bool waited = false;
-                while (ok && u.next(mt, kb0, kb1)) {
-                    if (!waited) {
-                        if (!grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) { ok = false; break; }
-                        fence_proxy_async_global();
-                        waited = true;
+        const uint64_t pol = policy_evict_last();
+        int stage = 0;
+        uint32_t par = 0;
+        int last_par[C::STAGES];
+        for (int s = 0; s < C::STAGES; ++s) last_par[s] = -1;
+        bool ok = true;
+        for (int k = 1; k < n_phases && ok; ++k) {
+            const Phase ph = phase_of(mp, p, k);
+            const int halves = ph.kind == K_GATEUP ? 2 : 1;
+            Units u(ph, G, cta);
+            int mt, kb0, kb1;
+            while (ok && u.next(mt, kb0, kb1)) {
+                for (int kb = kb0; ok && kb < kb1;) {
+                    int n = kb1 - kb;
+                    if (ph.src_kind >= 0) {
+                        n = ready_prefix(p, ph, kb, kb1, lane, labort, gabort);
+                        if (n == 0) { ok = false; break; }
                     }
-                    for (int kb = kb0; kb < kb1 && ok; ++kb) {
-                        for (int hf = 0; hf < halves; ++hf) {
-                            if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort)) { ok = false; break; }
-                            const uint32_t fb = smem_addr(&full_x[stage]);
-                            if (hf == 0) {
-                                mbar_expect_tx(fb, C::X_BYTES);
-                                tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, kb * 64, 0,
-                                              pol);
-                            } else {
-                                mbar_arrive(fb);
+                    if (lane == 0) {
+                        for (int j = 0; j < n && ok; ++j) {
+                            for (int hf = 0; hf < halves; ++hf) {
+                                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
+                                const uint32_t fb = smem_addr(&full_x[stage]);
+                                if (hf == 0) {
+                                    mbar_expect_tx(fb, C::X_BYTES);
+                                    tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb,
+                                                  (kb + j) * 64, 0, pol);
+                                } else {
+                                    mbar_arrive(fb);
+                                }
+                                last_par[stage] = (int)par;
+                                if (++stage == C::STAGES) { stage = 0; par ^= 1; }
                             }
-                            last_par[stage] = (int)par;
-                            if (++stage == C::STAGES) { stage = 0; par ^= 1; }
                         }
                     }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                    kb += n;
                 }
             }
-            if (!ok) {
-                fail();
-                for (int s = 0; s < C::STAGES; ++s) {
-                    if (last_par[s] < 0) continue;
-                    const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(smem_addr(&full_x[s]), (uint32_t)last_par[s]) &&
-                           globaltimer() - t0 < kWaitLimitNs) {}
-                }
+        }
+        if (!ok && lane == 0) {
+            fail();
+            for (int s = 0; s < C::STAGES; ++s) {
+                if (last_par[s] < 0) continue;
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(smem_addr(&full_x[s]), (uint32_t)last_par[s]) &&
+                       globaltimer() - t0 < kWaitLimitNs) {}
             }
         }
     } else if (warp == kWarpMma) {
@@ -402,12 +503,12 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 int mt, kb0, kb1;
                 while (ok && u.next(mt, kb0, kb1)) {
                     const int a = uc & 1;
-                    if (!mbar_wait(smem_addr(&acc_empty[a]), ((uc >> 1) & 1) ^ 1, labort, gabort)) { ok = false; break; }
+                    if (!mbar_wait(smem_addr(&acc_empty[a]), ((uc >> 1) & 1) ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d = tmem + a * kAccStride;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(smem_addr(&full_w[stage]), par, labort, gabort) ||
-                            !mbar_wait(smem_addr(&full_x[stage]), par, labort, gabort)) { ok = false; break; }
+                        if (!mbar_wait(smem_addr(&full_w[stage]), par, labort, gabort, p.wait_ns) ||
+                            !mbar_wait(smem_addr(&full_x[stage]), par, labort, gabort, p.wait_ns)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sw = smem_addr(smem + stage * C::STAGE);
                         const uint32_t sx = sw + C::W_BYTES;
@@ -419,7 +520,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                         uint32_t p2 = par;
                         if (s2 == C::STAGES) { s2 = 0; p2 ^= 1; }
                         if (dual) {
-                            if (!mbar_wait(smem_addr(&full_w[s2]), p2, labort, gabort)) { ok = false; break; }
+                            if (!mbar_wait(smem_addr(&full_w[s2]), p2, labort, gabort, p.wait_ns)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t sw2 = smem_addr(smem + s2 * C::STAGE);
 #pragma unroll
@@ -457,11 +558,13 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         const int q = warp & 3;
         const int row = q * 32 + lane;                 // drain: row of the tile (TMEM lane)
         const bool leader = warp == 2 && lane == 0;
+        const bool helper = warp == 3 && lane == 0;    // waits for the previous phase beside the leader
         const int B = p.B, D = p.D;
         const int Dt = (D + 127) / 128;
         bool dead = false;
 
         // phase 0: tile sums of squares of the launch input (warp per token)
+        unsigned n0 = 0;
         for (int mt = cta; mt < Dt; mt += G) {
             for (int t = q; t < B; t += 4) {
                 float ss = 0.f;
@@ -475,16 +578,17 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 ss = warp_sum32(ss);
                 if (lane == 0) p.slots_y[mt * B + t] = ss;
             }
+            n0 += (unsigned)B;
         }
         epi_sync();
-        if (leader) red_release_add(p.bar, 1u);
+        if (leader && n0) red_release_add(p.done, n0);
 
+        const size_t region = (size_t)(kFusedGridCap + p.max_mt);    // partial slots per projection kind
         int uc = 0;
         for (int k = 1; k < n_phases; ++k) {
             const Phase ph = phase_of(mp, p, k);
             const bool dual = ph.kind == K_GATEUP;
             const int planes = dual ? 2 : 1;
-            const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
             const int l = ph.layer;
             // parallel block: o_proj and down partials of a tile are added
             // together (one reduction for both sublayers), so they share the
@@ -493,31 +597,17 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const int tk_kind = (p.parallel && ph.kind == K_OPROJ) ? K_DOWN : ph.kind;
             Units u(ph, G, cta);
             int mt, kb0, kb1;
-            if (normed && u.idx < u.hi) {
-                // RMSNorm scales of the phase input, while the first unit's
-                // MMAs run: every tile sum was written before this phase's
-                // grid barrier; thread per token
-                if (leader && !dead && !grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) fail();
-                epi_sync();
-                // the serial block's MLP normalises h, everything else the layer input
-                const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
-                for (int t = row; t < B; t += 128) {
-                    float s = 0.f;
-#pragma unroll 4
-                    for (int m2 = 0; m2 < Dt; ++m2) s += __ldcg(sl + m2 * B + t);
-                    scale[t] = 1.0f / sqrtf(s / (float)D + p.eps);
-                }
-            }
+            const int first_uc = uc;
             // pass 1: drain every unit into its partial slot and count it on
             // its tile's ticket (no waiting here, so tiles never wait on one
             // another through a CTA that holds pieces of two of them)
             while (u.next(mt, kb0, kb1)) {
                 const int a = uc & 1;
                 dead = dead || *labort || *gabort;
-                const bool got = dead ? false : mbar_wait(smem_addr(&acc_full[a]), (uc >> 1) & 1, labort, gabort);
+                const bool got = dead ? false : mbar_wait(smem_addr(&acc_full[a]), (uc >> 1) & 1, labort, gabort, p.wait_ns);
                 dead = !__all_sync(0xFFFFFFFFu, got);
                 if (dead && lane == 0) fail();
-                float* slot = p.part + ((size_t)ph.region * (kFusedGridCap + p.max_mt) + cta + mt) * C::PART_FLOATS;
+                float* slot = p.part + ((size_t)ph.kind * region + cta + mt) * C::PART_FLOATS;
                 if (!dead) {
                     tc_fence_after();
                     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
@@ -537,8 +627,10 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (lane == 0) mbar_arrive(smem_addr(&acc_empty[a]));
                 ++uc;
                 epi_sync();                     // this CTA's partial of the tile is written
-                if (leader && !dead) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
+                const bool skip = cta == p.skip_cta && k == p.skip_phase && uc == first_uc + 1;
+                if (leader && !dead && !skip) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
             }
+            if (p.parallel && ph.kind == K_OPROJ) continue;    // finalized with down
             // pass 2: once all of a tile's units have arrived (a tile ticket
             // counts arrivals monotonically over the layers of the launch),
             // the CTAs holding them (contiguous, skipping CTAs without work)
@@ -566,9 +658,12 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 return cl_;
             };
             const Phase ph_o = merged ? phase_of(mp, p, k - 1) : ph;       // the o_proj phase of the layer
-            const size_t r1 = (size_t)(kFusedGridCap + p.max_mt);           // first slot of region 1
+            const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
+            // the serial block's MLP normalises h, everything else the layer input
+            const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
+            bool prev_done = ph.prev_fin < 0;
             Units u2(ph, G, cta);
-            while (!(p.parallel && ph.kind == K_OPROJ) && u2.next(mt, kb0, kb1)) {
+            while (u2.next(mt, kb0, kb1)) {
                 int cf, cf_o = 0;
                 bool every, every_o = true;
                 const int cl = seg_list(ph, mt, seg, 0, cf, every);
@@ -579,21 +674,28 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const int jseg = every ? cta - cf : seg_info[1];
                 const int nseg_o = !merged ? 0 : (every_o ? cl_o - cf_o + 1 : seg_info[2]);
                 const int nseg = nseg_o + nseg_d;
-                // slot of segment j: the o_proj segments (region 1) first, then
-                // this phase's own, each in k order
+                // slot of segment j: the o_proj segments first, then this
+                // phase's own, each in k order
                 auto slot_of = [&](int j) -> size_t {
-                    if (j < nseg_o) return r1 + (size_t)(every_o ? cf_o + j + mt : seg2[j]);
+                    if (j < nseg_o) return (size_t)K_OPROJ * region + (size_t)(every_o ? cf_o + j + mt : seg2[j]);
                     const int jd = j - nseg_o;
-                    return (size_t)ph.region * r1 + (size_t)(every ? cf + jd + mt : seg[jd]);
+                    return (size_t)ph.kind * region + (size_t)(every ? cf + jd + mt : seg[jd]);
                 };
 
                 // this CTA's share of the tile's tokens (none for most CTAs
                 // when B is small: those do not wait for the tile)
                 const int t_lo = (int)((int64_t)B * jseg / nseg_d), t_hi = (int)((int64_t)B * (jseg + 1) / nseg_d);
                 if (t_lo == t_hi) { epi_sync(); continue; }
+                // every unit of the tile has arrived, and the phase finalized
+                // before this one is complete (so are all earlier ones: each
+                // waited likewise); two threads wait side by side
                 if (leader && !dead &&
-                    !grid_wait(p.tickets + tk_kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort))
+                    !grid_wait(p.tickets + tk_kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort, p.wait_ns))
                     fail();
+                if (helper && !dead && !prev_done &&
+                    !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns))
+                    fail();
+                prev_done = true;
                 epi_sync();                     // every segment of the tile is visible
                 if (dead || *labort) { epi_sync(); continue; }
 
@@ -605,16 +707,14 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 __nv_bfloat16* dst = ph.kind == K_OPROJ ? p.h : (l == p.L - 1 ? p.y_out : ((l & 1) ? p.R1 : p.R0));
                 const float* pbase = p.part + lane * 4;     // + slot * PART_FLOATS
                 const bool has_resid = ph.kind == K_OPROJ || ph.kind == K_DOWN;
-                auto emit = [&](int t, const float4& acc, const float4& acc2, const uint2& rv) {
+                auto emit = [&](int t, const float4& acc, const float4& acc2, const uint2& rv, float s) {
                     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
                     if (ph.kind == K_QKV) {
-                        const float s = scale[t];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (r0 + e < p.n_qkv) store_qkv(p.qkv, t, r0 + e, av[e] * s, 1);
                     } else if (ph.kind == K_GATEUP) {
                         if (r0 < p.F) {
-                            const float s = scale[t];
                             const float uv[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
                             __nv_bfloat16 hb[4];
 #pragma unroll
@@ -649,23 +749,31 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
                 // A warp takes TB of its tokens at a time with up to SB segment
                 // loads in flight per token (per plane for gate/up), plus the
-                // residuals; segments are added in k order.  One token with 16
+                // residuals, or the token's RMSNorm tile sums (lanes over the
+                // tiles, summed lane-strided then by a butterfly: a fixed
+                // order); segments are added in k order.  One token with 16
                 // loads suits few tokens and many segments (NP = 16); two
                 // tokens per round trip suit the larger batches.
-                auto share = [&](auto tb_c, auto sb_c, auto dual_c) {
+                auto share = [&](auto tb_c, auto sb_c, auto dual_c, auto norm_c) {
                     constexpr int TB = decltype(tb_c)::value, SB = decltype(sb_c)::value;
-                    constexpr bool DU = decltype(dual_c)::value;
+                    constexpr bool DU = decltype(dual_c)::value, NO = decltype(norm_c)::value;
                     for (int t0 = t_lo + q; t0 < t_hi; t0 += 4 * TB) {
                         float4 acc[TB], acc2[TB];
                         uint2 rv[TB];
+                        float ssq[TB];
 #pragma unroll
                         for (int j = 0; j < TB; ++j) {
                             acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                             acc2[j] = acc[j];
                             rv[j] = make_uint2(0u, 0u);
+                            ssq[j] = 0.f;
                             const int t = t0 + 4 * j;
                             if (has_resid && t < t_hi && r0 < D)
                                 rv[j] = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
+                            if constexpr (NO) {
+                                if (t < t_hi)
+                                    for (int m2 = lane; m2 < Dt; m2 += 32) ssq[j] += __ldcg(sl + m2 * B + t);
+                            }
                         }
                         for (int s0 = 0; s0 < nseg; s0 += SB) {
                             float4 v[TB][SB], w[DU ? TB : 1][DU ? SB : 1];
@@ -691,8 +799,11 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                     }
                         }
 #pragma unroll
-                        for (int j = 0; j < TB; ++j)
-                            if (t0 + 4 * j < t_hi) emit(t0 + 4 * j, acc[j], acc2[j], rv[j]);
+                        for (int j = 0; j < TB; ++j) {
+                            float sc = 1.f;
+                            if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq[j]) / (float)D + p.eps);
+                            if (t0 + 4 * j < t_hi) emit(t0 + 4 * j, acc[j], acc2[j], rv[j], sc);
+                        }
                     }
                 };
                 using I1 = std::integral_constant<int, 1>;
@@ -700,29 +811,23 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 using I4 = std::integral_constant<int, 4>;
                 using I8 = std::integral_constant<int, 8>;
                 using I16 = std::integral_constant<int, 16>;
+                using T = std::true_type;
+                using Fa = std::false_type;
                 if constexpr (NP == 16) {
-                    if (!dual) share(I1{}, I16{}, std::false_type{}); else share(I1{}, I8{}, std::true_type{});
+                    if (dual) share(I1{}, I8{}, T{}, T{});
+                    else if (normed) share(I1{}, I16{}, Fa{}, T{});
+                    else share(I1{}, I16{}, Fa{}, Fa{});
                 } else {
-                    if (!dual) share(I2{}, I8{}, std::false_type{}); else share(I2{}, I4{}, std::true_type{});
+                    if (dual) share(I2{}, I4{}, T{}, T{});
+                    else if (normed) share(I2{}, I8{}, Fa{}, T{});
+                    else share(I2{}, I8{}, Fa{}, Fa{});
                 }
-                // (the next phase reads these outputs with TMA: its activation
-                // producer acquires the grid barrier, which this CTA releases
-                // after these stores, and then fences the async proxy)
-                epi_sync();                     // seg[] is rewritten for the next tile
-            }
-            // This CTA's part of phase k is done (including its token shares);
-            // after the last phase of a stage it signals the stage.  The
-            // counter counts completions of all stages, so a CTA signals stage
-            // s only once barrier s has passed (a CTA with no work in a stage
-            // gets here without having waited for it): then bar >= G (s+1)
-            // means that every CTA has finished stages 0..s.
-            epi_sync();
-            if (ph.last_of_stage && leader && !dead) {
-                if (grid_wait(p.bar, (unsigned)G * (unsigned)ph.stage, labort, gabort)) {
-                    red_release_add(p.bar, 1u);
-                } else {
-                    fail();
-                }
+                // this CTA's share of the tile is written: count it on the
+                // tile (the next phase's activation loads wait for that) and
+                // on the phase
+                epi_sync();
+                if (leader && !dead)
+                    publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)(t_hi - t_lo));
             }
         }
     }
@@ -738,6 +843,11 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
 
 int np_for(int64_t B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : 128; }
 
+// Test hook state (set by tpl_test_fused_fault): the next launches' wait
+// limit and the CTA / phase whose first ticket arrival is left out.
+std::atomic<int> g_skip_cta{-1}, g_skip_phase{-1};
+std::atomic<long long> g_wait_ns{0};
+
 template <int NP>
 int fused_smem() { return FCfg<NP>::SMEM; }
 
@@ -752,7 +862,8 @@ int smem_for(int np) {
 
 struct FusedPlan {
     int np, max_mt;
-    size_t ctrl_off, tick_off, sy_off, sh_off, r0_off, r1_off, o_off, h_off, hid_off, qkv_off, part_off, total;
+    size_t ctrl_off, tick_off, ready_off, done_off, sy_off, sh_off, r0_off, r1_off, o_off, h_off, hid_off, qkv_off,
+        part_off, total;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -768,8 +879,11 @@ FusedPlan plan_fused(const FusedShape& s) {
     const int kv_s = s.tp <= s.n_kv ? s.n_kv / s.tp : 1;
     const int64_t w_s = (int64_t)(s.n_q / s.tp + 2 * kv_s) * s.hd;
     size_t o = 0;
+    // control words, tickets, ready and done counters: zeroed before each launch
     f.ctrl_off = o; o += 256;
     f.tick_off = o; o += up256((size_t)4 * f.max_mt * 4);
+    f.ready_off = o; o += up256((size_t)4 * f.max_mt * 4);
+    f.done_off = o; o += up256((size_t)(1 + 4 * kFusedMaxLayers) * 4);
     f.sy_off = o; o += up256((size_t)Dt * s.B * 4);
     f.sh_off = o; o += up256((size_t)Dt * s.B * 4);
     f.r0_off = o; o += up256((size_t)s.B * s.D * 2);
@@ -778,8 +892,8 @@ FusedPlan plan_fused(const FusedShape& s) {
     f.h_off = o; o += up256((size_t)s.B * s.D * 2);
     f.hid_off = o; o += up256((size_t)s.B * s.F * 2);
     f.qkv_off = o; o += up256((size_t)s.tp * s.B * w_s * 2);
-    // two regions of partial slots (the parallel block runs two phases per stage)
-    f.part_off = o; o += up256((size_t)2 * (kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
+    // one region of partial slots per projection kind
+    f.part_off = o; o += up256((size_t)4 * (kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
     f.total = o;
     return f;
 }
@@ -802,9 +916,15 @@ cudaError_t launch_np(const FusedMaps& maps, const FusedParams& prm, cudaStream_
 
 }  // namespace
 
+void fused_test_fault(int cta, int phase, long long wait_ns) {
+    g_skip_cta = cta;
+    g_skip_phase = phase;
+    g_wait_ns = wait_ns;
+}
+
 bool fused_stack_shape_ok(const FusedShape& s) {
     if (s.B < 1 || s.B > 128) return false;
-    if (s.D % 64 || s.F % 64 || ((int64_t)s.n_q * s.hd) % 64) return false;
+    if (s.D % 64 || s.F % 64 || s.hd % 64) return false;
     return s.D <= (1 << 20) && s.F <= (1 << 20) && (int64_t)(s.n_q + 2 * s.n_kv) * s.hd <= (1 << 20);
 }
 
@@ -861,9 +981,13 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
     prm.slots_h = reinterpret_cast<float*>(w + f.sh_off);
     prm.part = reinterpret_cast<float*>(w + f.part_off);
     prm.tickets = reinterpret_cast<unsigned*>(w + f.tick_off);
-    prm.bar = reinterpret_cast<unsigned*>(w + f.ctrl_off);
-    prm.gabort = reinterpret_cast<int*>(w + f.ctrl_off + 4);
+    prm.ready = reinterpret_cast<unsigned*>(w + f.ready_off);
+    prm.done = reinterpret_cast<unsigned*>(w + f.done_off);
+    prm.gabort = reinterpret_cast<int*>(w + f.ctrl_off);
     prm.err = ctx->err_word;
+    prm.wait_ns = g_wait_ns > 0 ? (uint64_t)g_wait_ns : kWaitLimitNs;
+    prm.skip_cta = g_skip_cta;
+    prm.skip_phase = g_skip_phase;
     prm.y_out = static_cast<__nv_bfloat16*>(y);
 
     FusedMaps maps;
@@ -890,7 +1014,7 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
                 !tma_map_bf16(&maps.w[l][W_D], Wd[l0 + l], s.D, s.F, s.F, 128))
                 return cudaErrorInvalidValue;
         }
-        // grid barrier counter, abort flag and tickets start at zero
+        // abort flag, tickets, ready and done counters start at zero
         cudaError_t e = cudaMemsetAsync(w + f.ctrl_off, 0, f.sy_off - f.ctrl_off, st);
         if (e != cudaSuccess) return e;
         switch (np) {

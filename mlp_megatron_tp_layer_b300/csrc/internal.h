@@ -188,6 +188,8 @@ struct FusedShape {
 // Shapes the fused decode stack handles (B <= 128, widths multiples of 64).
 bool fused_stack_shape_ok(const FusedShape& s);
 size_t fused_stack_ws_bytes(const FusedShape& s);
+// Test hook behind tpl_test_fused_fault (cta < 0: off; wait_ns <= 0: default limit).
+void fused_test_fault(int cta, int phase, long long wait_ns);
 // The whole stack in persistent cooperative launches (kFusedMaxLayers layers each).
 // parallel: the parallel (PaLM) block y = x + Attn(RMSNorm(x)) + MLP(RMSNorm(x)).
 cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, const void* const* Wqkv,

@@ -50,22 +50,23 @@ static __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) 
 // time limit passes or another role (of this CTA: abort_flag; of any CTA:
 // abort_flag2, may be null) has already aborted.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                   volatile int* abort_flag2) {
+                                                   volatile int* abort_flag2, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag || (abort_flag2 && *abort_flag2)) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
         }
     }
 }
 // A phase that has already completed is found by the inline non-blocking test,
 // without the call and the blocking try-wait (measured: a few hundred cycles).
 static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                 volatile int* abort_flag2 = nullptr) {
-    return mbar_test(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, abort_flag2);
+                                                 volatile int* abort_flag2 = nullptr,
+                                                 uint64_t limit_ns = kWaitLimitNs) {
+    return mbar_test(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, abort_flag2, limit_ns);
 }
 
 static __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -89,6 +90,12 @@ static __device__ __forceinline__ void tma_load_hint(uint32_t dst, const CUtenso
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+// Bring one box of a tiled tensor into L2 (no shared-memory destination, no
+// completion to wait for): later TMA loads of it hit L2 instead of DRAM.
+static __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
 }
 static __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
