@@ -64,6 +64,8 @@ def args_parse():
     ap.add_argument("--no-cases", action="store_true", help="skip the sharded-matmul cases and shard_reduce")
     ap.add_argument("--no-lm-head", action="store_true", help="skip the vocabulary-parallel lm_head lines")
     ap.add_argument("--no-w8", action="store_true", help="skip the weight-only int8 MLP lines")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip timing the unfused decode path beside the fused one")
     ap.add_argument("--model", "--lm-head-model", dest="model", choices=["llama-3.1-70b", "qwen2.5-1.5b"],
                     default=None, help="with --only lm_head or --only w8: one model's shape only "
                                        "(--batches selects the batch sizes)")
@@ -479,6 +481,20 @@ def run_decode(args, tpl, dev, world, peaks, peak_kind, stream):
             agg[tag] = (n + 1, s_ + t)
         per_batch[str(B)]["kernel_us"] = {k: round(v[1] / v[0] * 1e3, 2) for k, v in agg.items()}
         per_batch[str(B)]["sum_kernel_us_per_layer"] = round(sum(v[1] for v in agg.values()) / L * 1e3, 2)
+    # the unfused path (one launch per projection and reduction, graph-
+    # replayed) beside the fused one, per batch size: what the automatic path
+    # choice rests on
+    if not args.no_unfused:
+        for B in batches:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws, path=tpl.PATH_UNFUSED)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws, path=tpl.PATH_UNFUSED)
+            t = time_ms(g.replay, max(3, args.steps // 4))
+            per_batch[str(B)]["unfused"] = {"ms_per_forward": t, "GB/s": L * QWEN_LAYER_BYTES / (t / 1e3) / 1e9}
+            del g
     out = {"value": value, "ms": ms, "batches": batches, "L": L, "roofline": roof, "e2e": e2e,
            "gpu_launches": launches_per_step * args.steps, "clocks": clk, "per_batch": per_batch,
            "kernel_share": share, "layers": layers}
@@ -548,6 +564,18 @@ def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
         t = a.elapsed_time(b) / reps
         gbs = L * LLAMA_LAYER_BYTES / (t / 1e3) / 1e9
         out["per_batch"][str(B)] = {"ms_per_forward": t, "GB/s": gbs, "frac_of_peak": gbs / peaks["hbm_gbs"]}
+    if not args.no_unfused:
+        for B in batches:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws, path=tpl.PATH_UNFUSED)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                tpl.tp_decoder_stack(xs[B], layers, n_q, n_kv, hd, tp, out=ys[B], ws=ws, path=tpl.PATH_UNFUSED)
+            t = time_ms(g.replay, reps)
+            out["per_batch"][str(B)]["unfused"] = {"ms_per_forward": t,
+                                                   "GB/s": L * LLAMA_LAYER_BYTES / (t / 1e3) / 1e9}
+            del g
     del layers, graphs
     torch.cuda.empty_cache()
     return out

@@ -250,3 +250,12 @@ def test_static_scratch_limit_uses_the_calls_own_plan_and_dtype_comes_first():
     n = ctypes.c_size_t(0)
     lib.tpl_tp_mlp_forward_workspace(32, D, F, tp, tpl.BF16, ctypes.byref(n))
     assert n.value <= tpl.STATIC_WS_BYTES
+
+
+def test_fused_fault_hook_checks_its_arguments():
+    assert lib.tpl_test_fused_fault(-1, 1, 0) == 0                       # defaults
+    assert tpl.STATUS[lib.tpl_test_fused_fault(3, 0, 0)] == "TPL_ERR_UNSUPPORTED"        # phase 0 has no units
+    assert tpl.STATUS[lib.tpl_test_fused_fault(148, 1, 0)] == "TPL_ERR_UNSUPPORTED"      # beyond the grid
+    assert tpl.STATUS[lib.tpl_test_fused_fault(-1, 1, 5000)] == "TPL_ERR_UNSUPPORTED"    # under 10 us
+    assert tpl.STATUS[lib.tpl_test_fused_fault(-1, 1, 3_000_000_000)] == "TPL_ERR_UNSUPPORTED"
+    assert lib.tpl_test_fused_fault(-1, 1, 0) == 0

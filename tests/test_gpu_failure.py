@@ -1,0 +1,86 @@
+"""The failure path of the fused decode stack, exercised without a fault.
+
+The pages' TP serving hang modes are a collective that never completes
+because one rank never arrives.  Here the stand-in for a rank is a CTA, and
+the collective is a tile's split-K reduction: with the library's test hook a
+CTA leaves out one ticket arrival, so the tile's finalize waits until its
+(shortened) time limit passes.  The launch must then end by itself (every
+wait bounded, every CTA winding down through the abort flag), report
+TPL_DEVERR_TIMEOUT in the device error word, and leave nothing behind: the
+next normal call on the same workspace equals a fresh one bit for bit."""
+import time
+
+import pytest
+import torch
+
+import synthetic_inputs as si
+
+pytestmark = pytest.mark.gpu
+tpl = pytest.importorskip("mlp_megatron_tp_layer_b300")
+
+TIMEOUT_BIT = 0x1   # TPL_DEVERR_TIMEOUT
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.synchronize()
+    tpl.device_status()
+    yield
+    tpl.test_fused_fault()
+    torch.cuda.synchronize()
+    assert tpl.device_status() == 0
+
+
+# D 1024, F 2048: gate/up and down have 256 (m-tile, k-block) pairs, so every
+# one of the 148 CTAs holds work there; the last CTA holds work in every phase.
+SHAPE = dict(D=1024, F=2048, n_q=8, n_kv=2, hd=128, tp=2, L=2)
+
+
+def _stack(B, block):
+    s = SHAPE
+    layers = [si.layer_weights(s["D"], s["F"], s["n_q"], s["n_kv"], s["hd"], seed=31, layer=l, sigma=0.03,
+                               device="cuda") for l in range(s["L"])]
+    x = si.activations(B, s["D"], seed=31, device="cuda")
+
+    def run():
+        return tpl.tp_decoder_stack(x, layers, s["n_q"], s["n_kv"], s["hd"], s["tp"], path=tpl.PATH_FUSED,
+                                    block=block)
+    return run
+
+
+# (cta, phase): phase 4 l + 1 + j is projection j of layer l in the block's order
+@pytest.mark.parametrize("B,block,cta,phase", [
+    (1, tpl.BLOCK_SERIAL, 147, 1),       # QKV of layer 0
+    (40, tpl.BLOCK_SERIAL, 0, 3),        # gate/up of layer 0
+    (1, tpl.BLOCK_SERIAL, 147, 8),       # down of layer 1
+    (16, tpl.BLOCK_PARALLEL, 147, 3),    # o_proj, finalized together with down
+])
+def test_fused_stack_wait_runs_out_and_the_next_call_is_clean(B, block, cta, phase):
+    run = _stack(B, block)
+    ref = run()
+    assert tpl.device_status() == 0
+    tpl.test_fused_fault(cta, phase, 1_000_000)          # 1 ms limit
+    t0 = time.perf_counter()
+    run()                                                # the launch itself succeeds
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    flags = tpl.device_status()
+    tpl.test_fused_fault()
+    assert flags & TIMEOUT_BIT, f"expected a timed-out wait, flags={flags:#x}"
+    assert dt < 1.0, f"the aborted launch took {dt:.3f} s"
+    again = run()
+    torch.cuda.synchronize()
+    assert tpl.device_status() == 0
+    assert torch.equal(again, ref), "the call after the aborted one differs from a fresh call"
+
+
+def test_short_wait_limit_alone_changes_nothing():
+    run = _stack(8, tpl.BLOCK_SERIAL)
+    ref = run()
+    tpl.test_fused_fault(-1, 1, 50_000_000)              # 50 ms, nothing left out
+    y = run()
+    torch.cuda.synchronize()
+    assert tpl.device_status() == 0
+    assert torch.equal(y, ref)
