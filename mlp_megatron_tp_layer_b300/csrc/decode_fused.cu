@@ -62,15 +62,13 @@ namespace tpl {
 namespace {
 
 constexpr int kFThreads = 224;
-#ifndef TPL_FUSED_PREFETCH
-#define TPL_FUSED_PREFETCH 0
-#endif
-constexpr int kFusedPrefetch = TPL_FUSED_PREFETCH;   // weight tiles prefetched to L2 ahead of the ring
+constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory of one CTA
+constexpr int kFinItems = 10;              // float4 rows (of 32 lanes) a finalizing warp stages at once
 constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
 enum Kind { K_QKV = 0, K_OPROJ = 1, K_GATEUP = 2, K_DOWN = 3 };
-enum ActMap { A_X = 0, A_R0 = 1, A_R1 = 2, A_O = 3, A_H = 4, A_HID = 5, A_COUNT = 6 };
+enum ActMap { A_X = 0, A_R0 = 1, A_R1 = 2, A_QKV = 3, A_H = 4, A_HID = 5, A_COUNT = 6 };
 enum WMap { W_QKV = 0, W_O = 1, W_G = 2, W_U = 3, W_D = 4, W_COUNT = 5 };
 
 // Tensor maps travel as a __grid_constant__ kernel parameter (about 21 KB).
@@ -85,9 +83,9 @@ struct FusedParams {
     int n_qkv, ko;             // packed QKV rows, o_proj input width n_q hd
     int max_mt;                // length of a ticket / ready row
     float eps;
-    QkvMap qkv;                // packed-QKV scatter (qkv_out = shard blocks, o_out = O)
+    QkvMap qkv;                // packed-QKV layout (qkv_out = shard blocks [tp, B, w_s])
     const __nv_bfloat16* x_in;
-    __nv_bfloat16 *y_out, *R0, *R1, *O, *h, *H;
+    __nv_bfloat16 *y_out, *R0, *R1, *h, *H;
     float* slots_y;            // [ceil(D/128)][B] sums of squares of the layer input / output
     float* slots_h;            // [ceil(D/128)][B] sums of squares of h
     float* part;               // partial tiles, [4 kinds][G + max_mt][2][NP][128] fp32
@@ -105,16 +103,18 @@ struct FCfg {
     static constexpr int W_BYTES = 128 * 64 * 2;                 // one 128 x 64 weight tile
     static constexpr int X_BYTES = NP * 64 * 2;                  // the NP x 64 activation tile
     static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
-    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int CTRL = 1024;                            // mbarriers and flags
     static constexpr int EPI = (2 * kFusedGridCap + 8) * 4;     // two segment lists and their counts
-    static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI;
+    static constexpr int FIN = 4 * kFinItems * 32 * 16;          // finalize staging, per epilogue warp
+    static constexpr int STAGES_RAW = (kSmemLimit - 1024 - CTRL - EPI - FIN) / STAGE;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI + FIN;
     static constexpr int PART_FLOATS = 2 * NP * 128;             // one partial slot
     static constexpr int CH = NP >= 32 ? 32 : 16;                // TMEM columns per load
     static_assert(NP % 16 == 0 && NP >= 16 && NP <= 128, "N of an M=128 MMA: 16..256, step 16");
     static_assert(STAGE % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
     static_assert(3 * STAGES + 5 <= 120, "mbarriers must fit the control block");
+    static_assert(STAGES >= 4, "too few ring stages");
 };
 
 struct Phase {
@@ -154,7 +154,7 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
         ph.M = p.n_qkv; K = p.D; wa = W_QKV;
         break;
     case K_OPROJ:
-        ph.M = p.D; K = p.ko; wa = W_O; ph.act = &mp.act[A_O];
+        ph.M = p.D; K = p.ko; wa = W_O; ph.act = &mp.act[A_QKV];
         ph.src_kind = K_QKV; ph.src_target = B * (unsigned)(l + 1);
         break;
     case K_GATEUP:
@@ -192,6 +192,28 @@ __device__ __forceinline__ unsigned done_target(const FusedMaps& mp, const Fused
 // g = h / (n_q / n_kv), i.e. packed-QKV rows (n_q + n_kv + g) hd + (64 kb mod hd)
 // (a 64-wide block never straddles two heads: hd % 64 == 0).  Every other
 // input is the previous phase's output read in place: 128-wide tile kb / 2.
+__device__ __forceinline__ int src_tile(const FusedParams& p, const Phase& ph, int kb);
+
+// Coordinates (x = column, y = first row) of k-block kb's activation tile.
+// o_proj's input is the context-1 attention output O, whose column block kb
+// (Q head h = 64 kb / hd) equals V of KV group g = h / (n_q / n_kv): it is
+// read in place from the shard-blocked QKV output [tp B, w_s], at the V
+// columns of the first shard holding group g (the TMA box's rows past that
+// shard's B tokens are other shards' rows, or zero fill past the end: they
+// only reach accumulator columns of padding tokens, which are never stored).
+// Every other input is [B, K] read at column 64 kb.
+__device__ __forceinline__ void act_coord(const FusedParams& p, const Phase& ph, int kb, int& x, int& y) {
+    if (ph.kind != K_OPROJ) { x = kb * 64; y = 0; return; }
+    const QkvMap& q = p.qkv;
+    const int col = kb * 64;
+    const int head = col / q.head_dim;
+    const int g = head / (q.n_q / q.n_kv);
+    const int s = q.tp <= q.n_kv ? g / q.kv_s : g * (q.tp / q.n_kv);
+    const int c = q.tp <= q.n_kv ? g - s * q.kv_s : 0;
+    x = (q.nq_s + q.kv_s + c) * q.head_dim + (col - head * q.head_dim);
+    y = s * p.B;
+}
+
 __device__ __forceinline__ int src_tile(const FusedParams& p, const Phase& ph, int kb) {
     if (ph.kind != K_OPROJ) return kb >> 1;
     const int hd = p.qkv.head_dim;
@@ -288,6 +310,44 @@ __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, vol
     }
 }
 
+// 16-byte global -> shared copy through L2 only (cp.async, no registers held
+// while it is in flight), and the wait for every copy this thread issued.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Packed-QKV rows r0 .. r0+3 (one head: hd % 64 == 0) of token t, rounded
+// to bf16, stored as one 8-byte word into every shard block that holds the
+// head (KV groups are replicated over shards when tp > n_kv).
+__device__ __forceinline__ void store_qkv4(const QkvMap& q, int t, int r0, float v0, float v1, float v2, float v3) {
+    const int hd = q.head_dim;
+    const int head = r0 / hd, d = r0 - head * hd;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v0, v1), hi = __floats2bfloat162_rn(v2, v3);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(q.qkv_out);
+    if (head < q.n_q) {
+        const int s = head / q.nq_s, j = head - s * q.nq_s;
+        *reinterpret_cast<uint2*>(out + s * q.shard_stride + (int64_t)t * q.w_s + (int64_t)j * hd + d) = w;
+        return;
+    }
+    const bool is_v = head >= q.n_q + q.n_kv;
+    const int g = head - q.n_q - (is_v ? q.n_kv : 0);
+    const int64_t col = (int64_t)(q.nq_s + (is_v ? q.kv_s : 0)) * hd + d;
+    if (q.tp <= q.n_kv) {
+        const int s = g / q.kv_s, c = g - s * q.kv_s;
+        *reinterpret_cast<uint2*>(out + s * q.shard_stride + (int64_t)t * q.w_s + col + (int64_t)c * hd) = w;
+    } else {
+        const int copies = q.tp / q.n_kv;
+        for (int s = g * copies; s < (g + 1) * copies; ++s)
+            *reinterpret_cast<uint2*>(out + s * q.shard_stride + (int64_t)t * q.w_s + col) = w;
+    }
+}
+
 // Release-publish two counter increments: every write this thread (and,
 // through a preceding barrier, its CTA) made is visible before either count.
 __device__ __forceinline__ void publish2(unsigned* a, unsigned* b, unsigned v) {
@@ -296,16 +356,23 @@ __device__ __forceinline__ void publish2(unsigned* a, unsigned* b, unsigned v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(b), "r"(v) : "memory");
 }
 
-// Warp-collective: how many of the k-blocks kb, kb+1, .. < kb1 (at most 32)
-// lead with their source tiles final, waiting until at least one is.  Lane j
-// polls the ready counter of k-block kb+j (acquire); the count returned is
-// the same in every lane.  0: the wait gave up (time limit or abort).  Every
-// lane then fences the async proxy, so the TMA loads issued after the warp
+// Warp-collective: how many of this CTA's (m-tile, k-block) pairs idx, idx+1,
+// .. < hi of phase ph (at most 32, flattened m-major like Units) lead with
+// the source tiles of their k-blocks final, waiting until at least one is.
+// Lane j polls the ready counter of pair idx+j (acquire; pairs of different
+// m-tiles with the same k-block read the same counter), so one round trip
+// usually covers a CTA's whole share of a phase.  The count returned is the
+// same in every lane; 0: the wait gave up (time limit or abort).  Every lane
+// then fences the async proxy, so the TMA loads issued after the warp
 // barrier see the tiles' contents.
-__device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& ph, int kb, int kb1, int lane,
-                                         volatile int* labort, volatile int* gabort) {
-    const int want = min(kb1 - kb, 32);
-    const unsigned* ctr = lane < want ? p.ready + ph.src_kind * p.max_mt + src_tile(p, ph, kb + lane) : nullptr;
+__device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& ph, int64_t idx, int64_t hi,
+                                            int lane, volatile int* labort, volatile int* gabort) {
+    const int want = (int)min(hi - idx, (int64_t)32);
+    const unsigned* ctr = nullptr;
+    if (lane < want) {
+        const int kb = (int)((idx + lane) % ph.nkb);
+        ctr = p.ready + ph.src_kind * p.max_mt + src_tile(p, ph, kb);
+    }
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
         bool r = true;
@@ -315,7 +382,7 @@ __device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& p
             r = v >= ph.src_target;
         }
         const unsigned m = __ballot_sync(0xFFFFFFFFu, r);
-        const int lead = __ffs(~m) == 0 ? 32 : __ffs(~m) - 1;     // leading ready k-blocks
+        const int lead = __ffs(~m) == 0 ? 32 : __ffs(~m) - 1;     // leading ready pairs
         const int n = min(want, lead);
         if (n > 0) {
             fence_proxy_async_global();
@@ -346,6 +413,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
     volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
     int* seg = reinterpret_cast<int*>(ctrl + C::CTRL);          // partial slots of the tile being finalized
+    float4* fin_buf = reinterpret_cast<float4*>(ctrl + C::CTRL + C::EPI);   // [4 warps][kFinItems][32 lanes]
     int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
     volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, jseg, nseg2, jseg2]
 
@@ -388,17 +456,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             TileCursor ld{};
-            // a second cursor runs kFusedPrefetch tiles ahead and brings those
-            // tiles into L2, so HBM keeps streaming while the ring is full
-            // (waiting for activations) and the ring's loads hit L2
-            TileCursor pf{};
-            bool pf_more = kFusedPrefetch > 0;
-            for (int i = 0; i < kFusedPrefetch && pf_more; ++i) {
-                const CUtensorMap* pm;
-                int px, py;
-                pf_more = pf.next(mp, p, G, cta, n_phases, pm, px, py);
-                if (pf_more) tma_prefetch_l2(pm, px, py);
-            }
             int stage = 0;
             uint32_t par = 0;
             int last_par[C::STAGES];           // parity of the latest copy issued into each stage, -1: none
@@ -411,12 +468,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const uint32_t fb = smem_addr(&full_w[stage]);
                 mbar_expect_tx(fb, C::W_BYTES);
                 tma_load_hint(smem_addr(smem + stage * C::STAGE), map, fb, x, y, pol);
-                if (pf_more) {
-                    const CUtensorMap* pm;
-                    int px, py;
-                    pf_more = pf.next(mp, p, G, cta, n_phases, pm, px, py);
-                    if (pf_more) tma_prefetch_l2(pm, px, py);
-                }
                 last_par[stage] = (int)par;
                 if (++stage == C::STAGES) { stage = 0; par ^= 1; }
             }
@@ -448,35 +499,34 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         for (int k = 1; k < n_phases && ok; ++k) {
             const Phase ph = phase_of(mp, p, k);
             const int halves = ph.kind == K_GATEUP ? 2 : 1;
-            Units u(ph, G, cta);
-            int mt, kb0, kb1;
-            while (ok && u.next(mt, kb0, kb1)) {
-                for (int kb = kb0; ok && kb < kb1;) {
-                    int n = kb1 - kb;
-                    if (ph.src_kind >= 0) {
-                        n = ready_prefix(p, ph, kb, kb1, lane, labort, gabort);
-                        if (n == 0) { ok = false; break; }
-                    }
-                    if (lane == 0) {
-                        for (int j = 0; j < n && ok; ++j) {
-                            for (int hf = 0; hf < halves; ++hf) {
-                                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
-                                const uint32_t fb = smem_addr(&full_x[stage]);
-                                if (hf == 0) {
-                                    mbar_expect_tx(fb, C::X_BYTES);
-                                    tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb,
-                                                  (kb + j) * 64, 0, pol);
-                                } else {
-                                    mbar_arrive(fb);
-                                }
-                                last_par[stage] = (int)par;
-                                if (++stage == C::STAGES) { stage = 0; par ^= 1; }
+            const Units u(ph, G, cta);            // this CTA's pairs [u.idx, u.hi), in k order per m-tile
+            for (int64_t idx = u.idx; ok && idx < u.hi;) {
+                int n = (int)min(u.hi - idx, (int64_t)32);
+                if (ph.src_kind >= 0) {
+                    n = ready_prefix(p, ph, idx, u.hi, lane, labort, gabort);
+                    if (n == 0) { ok = false; break; }
+                }
+                if (lane == 0) {
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int kb = (int)((idx + j) % ph.nkb);
+                        for (int hf = 0; hf < halves; ++hf) {
+                            if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
+                            const uint32_t fb = smem_addr(&full_x[stage]);
+                            if (hf == 0) {
+                                mbar_expect_tx(fb, C::X_BYTES);
+                                int ax, ay;
+                                act_coord(p, ph, kb, ax, ay);
+                                tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, ax, ay, pol);
+                            } else {
+                                mbar_arrive(fb);
                             }
+                            last_par[stage] = (int)par;
+                            if (++stage == C::STAGES) { stage = 0; par ^= 1; }
                         }
                     }
-                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-                    kb += n;
                 }
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                idx += n;
             }
         }
         if (!ok && lane == 0) {
@@ -710,9 +760,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 auto emit = [&](int t, const float4& acc, const float4& acc2, const uint2& rv, float s) {
                     const float av[4] = {acc.x, acc.y, acc.z, acc.w};
                     if (ph.kind == K_QKV) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (r0 + e < p.n_qkv) store_qkv(p.qkv, t, r0 + e, av[e] * s, 1);
+                        if (r0 < p.n_qkv) store_qkv4(p.qkv, t, r0, av[0] * s, av[1] * s, av[2] * s, av[3] * s);
                     } else if (ph.kind == K_GATEUP) {
                         if (r0 < p.F) {
                             const float uv[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
@@ -747,81 +795,57 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                 };
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
-                // A warp takes TB of its tokens at a time with up to SB segment
-                // loads in flight per token (per plane for gate/up), plus the
-                // residuals, or the token's RMSNorm tile sums (lanes over the
+                // A warp takes its tokens one at a time.  Each lane copies its
+                // own 16 bytes (4 rows) of every partial segment of the token
+                // (both planes for gate/up) into the warp's staging rows with
+                // cp.async, up to SB segments per batch, all in flight at
+                // once, and adds them from shared memory in k order; the
+                // residual, or the token's RMSNorm tile sums (lanes over the
                 // tiles, summed lane-strided then by a butterfly: a fixed
-                // order); segments are added in k order.  One token with 16
-                // loads suits few tokens and many segments (NP = 16); two
-                // tokens per round trip suit the larger batches.
-                auto share = [&](auto tb_c, auto sb_c, auto dual_c, auto norm_c) {
-                    constexpr int TB = decltype(tb_c)::value, SB = decltype(sb_c)::value;
+                // order), load alongside.
+                const uint32_t fb_s = smem_addr(fin_buf + q * (kFinItems * 32) + lane);
+                const float4* fb = fin_buf + q * (kFinItems * 32) + lane;
+                auto share = [&](auto dual_c, auto norm_c) {
                     constexpr bool DU = decltype(dual_c)::value, NO = decltype(norm_c)::value;
-                    for (int t0 = t_lo + q; t0 < t_hi; t0 += 4 * TB) {
-                        float4 acc[TB], acc2[TB];
-                        uint2 rv[TB];
-                        float ssq[TB];
-#pragma unroll
-                        for (int j = 0; j < TB; ++j) {
-                            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            acc2[j] = acc[j];
-                            rv[j] = make_uint2(0u, 0u);
-                            ssq[j] = 0.f;
-                            const int t = t0 + 4 * j;
-                            if (has_resid && t < t_hi && r0 < D)
-                                rv[j] = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
-                            if constexpr (NO) {
-                                if (t < t_hi)
-                                    for (int m2 = lane; m2 < Dt; m2 += 32) ssq[j] += __ldcg(sl + m2 * B + t);
-                            }
+                    constexpr int PL = DU ? 2 : 1;
+                    constexpr int SB = kFinItems / PL;
+                    for (int t = t_lo + q; t < t_hi; t += 4) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+                        uint2 rv = make_uint2(0u, 0u);
+                        float ssq = 0.f;
+                        if (has_resid && r0 < D) rv = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
+                        if constexpr (NO) {
+                            for (int m2 = lane; m2 < Dt; m2 += 32) ssq += __ldcg(sl + m2 * B + t);
                         }
                         for (int s0 = 0; s0 < nseg; s0 += SB) {
-                            float4 v[TB][SB], w[DU ? TB : 1][DU ? SB : 1];
+                            const int nb = min(SB, nseg - s0);
 #pragma unroll
-                            for (int j = 0; j < TB; ++j)
-#pragma unroll
-                                for (int k2 = 0; k2 < SB; ++k2) {
-                                    const int t = t0 + 4 * j;
-                                    if (t < t_hi && s0 + k2 < nseg) {
-                                        const float* sp = pbase + (size_t)slot_of(s0 + k2) * C::PART_FLOATS;
-                                        v[j][k2] = __ldcg(reinterpret_cast<const float4*>(sp + t * 128));
-                                        if constexpr (DU)
-                                            w[j][k2] = __ldcg(reinterpret_cast<const float4*>(sp + (NP + t) * 128));
-                                    }
+                            for (int k2 = 0; k2 < SB; ++k2) {
+                                if (k2 < nb) {
+                                    const float* sp = pbase + (size_t)slot_of(s0 + k2) * C::PART_FLOATS + t * 128;
+                                    cp_async16(fb_s + (uint32_t)(k2 * PL) * 512u, sp);
+                                    if constexpr (DU) cp_async16(fb_s + (uint32_t)(k2 * PL + 1) * 512u, sp + NP * 128);
                                 }
+                            }
+                            cp_async_wait_all();
 #pragma unroll
-                            for (int j = 0; j < TB; ++j)
-#pragma unroll
-                                for (int k2 = 0; k2 < SB; ++k2)
-                                    if (t0 + 4 * j < t_hi && s0 + k2 < nseg) {
-                                        add4(acc[j], v[j][k2]);
-                                        if constexpr (DU) add4(acc2[j], w[j][k2]);
-                                    }
+                            for (int k2 = 0; k2 < SB; ++k2) {
+                                if (k2 < nb) {
+                                    add4(acc, fb[(k2 * PL) * 32]);
+                                    if constexpr (DU) add4(acc2, fb[(k2 * PL + 1) * 32]);
+                                }
+                            }
                         }
-#pragma unroll
-                        for (int j = 0; j < TB; ++j) {
-                            float sc = 1.f;
-                            if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq[j]) / (float)D + p.eps);
-                            if (t0 + 4 * j < t_hi) emit(t0 + 4 * j, acc[j], acc2[j], rv[j], sc);
-                        }
+                        float sc = 1.f;
+                        if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq) / (float)D + p.eps);
+                        emit(t, acc, acc2, rv, sc);
                     }
                 };
-                using I1 = std::integral_constant<int, 1>;
-                using I2 = std::integral_constant<int, 2>;
-                using I4 = std::integral_constant<int, 4>;
-                using I8 = std::integral_constant<int, 8>;
-                using I16 = std::integral_constant<int, 16>;
                 using T = std::true_type;
                 using Fa = std::false_type;
-                if constexpr (NP == 16) {
-                    if (dual) share(I1{}, I8{}, T{}, T{});
-                    else if (normed) share(I1{}, I16{}, Fa{}, T{});
-                    else share(I1{}, I16{}, Fa{}, Fa{});
-                } else {
-                    if (dual) share(I2{}, I4{}, T{}, T{});
-                    else if (normed) share(I2{}, I8{}, Fa{}, T{});
-                    else share(I2{}, I8{}, Fa{}, Fa{});
-                }
+                if (dual) share(T{}, T{});
+                else if (normed) share(Fa{}, T{});
+                else share(Fa{}, Fa{});
                 // this CTA's share of the tile is written: count it on the
                 // tile (the next phase's activation loads wait for that) and
                 // on the phase
@@ -862,7 +886,7 @@ int smem_for(int np) {
 
 struct FusedPlan {
     int np, max_mt;
-    size_t ctrl_off, tick_off, ready_off, done_off, sy_off, sh_off, r0_off, r1_off, o_off, h_off, hid_off, qkv_off,
+    size_t ctrl_off, tick_off, ready_off, done_off, sy_off, sh_off, r0_off, r1_off, h_off, hid_off, qkv_off,
         part_off, total;
 };
 
@@ -872,7 +896,6 @@ FusedPlan plan_fused(const FusedShape& s) {
     FusedPlan f{};
     f.np = np_for(s.B);
     const int64_t n_qkv = (int64_t)(s.n_q + 2 * s.n_kv) * s.hd;
-    const int64_t ko = (int64_t)s.n_q * s.hd;
     const int64_t mts[4] = {(n_qkv + 127) / 128, (s.D + 127) / 128, (s.F + 127) / 128, (s.D + 127) / 128};
     f.max_mt = (int)*std::max_element(mts, mts + 4);
     const int64_t Dt = (s.D + 127) / 128;
@@ -888,7 +911,6 @@ FusedPlan plan_fused(const FusedShape& s) {
     f.sh_off = o; o += up256((size_t)Dt * s.B * 4);
     f.r0_off = o; o += up256((size_t)s.B * s.D * 2);
     f.r1_off = o; o += up256((size_t)s.B * s.D * 2);
-    f.o_off = o; o += up256((size_t)s.B * ko * 2);
     f.h_off = o; o += up256((size_t)s.B * s.D * 2);
     f.hid_off = o; o += up256((size_t)s.B * s.F * 2);
     f.qkv_off = o; o += up256((size_t)s.tp * s.B * w_s * 2);
@@ -970,11 +992,10 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
     prm.qkv.w_s = (int64_t)(prm.qkv.nq_s + 2 * kv_s) * s.hd;
     prm.qkv.shard_stride = s.B * prm.qkv.w_s;
     prm.qkv.qkv_out = w + f.qkv_off;
-    prm.qkv.o_out = w + f.o_off;
-    prm.qkv.ldo_o = ko;
+    prm.qkv.o_out = nullptr;
+    prm.qkv.ldo_o = 0;
     prm.R0 = reinterpret_cast<__nv_bfloat16*>(w + f.r0_off);
     prm.R1 = reinterpret_cast<__nv_bfloat16*>(w + f.r1_off);
-    prm.O = reinterpret_cast<__nv_bfloat16*>(w + f.o_off);
     prm.h = reinterpret_cast<__nv_bfloat16*>(w + f.h_off);
     prm.H = reinterpret_cast<__nv_bfloat16*>(w + f.hid_off);
     prm.slots_y = reinterpret_cast<float*>(w + f.sy_off);
@@ -995,7 +1016,7 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
     const int np = f.np;
     if (!tma_map_bf16(&maps.act[A_R0], prm.R0, s.B, s.D, s.D, np) ||
         !tma_map_bf16(&maps.act[A_R1], prm.R1, s.B, s.D, s.D, np) ||
-        !tma_map_bf16(&maps.act[A_O], prm.O, s.B, ko, ko, np) ||
+        !tma_map_bf16(&maps.act[A_QKV], prm.qkv.qkv_out, (int64_t)s.tp * s.B, prm.qkv.w_s, prm.qkv.w_s, np) ||
         !tma_map_bf16(&maps.act[A_H], prm.h, s.B, s.D, s.D, np) ||
         !tma_map_bf16(&maps.act[A_HID], prm.H, s.B, s.F, s.F, np))
         return cudaErrorInvalidValue;

@@ -91,12 +91,6 @@ static __device__ __forceinline__ void tma_load_hint(uint32_t dst, const CUtenso
         " [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
 }
-// Bring one box of a tiled tensor into L2 (no shared-memory destination, no
-// completion to wait for): later TMA loads of it hit L2 instead of DRAM.
-static __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
 static __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
