@@ -63,7 +63,6 @@ namespace {
 
 constexpr int kFThreads = 224;
 constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory of one CTA
-constexpr int kFinItems = 10;              // float4 rows (of 32 lanes) a finalizing warp stages at once
 constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
@@ -105,7 +104,8 @@ struct FCfg {
     static constexpr int STAGE = W_BYTES + X_BYTES;
     static constexpr int CTRL = 1024;                            // mbarriers and flags
     static constexpr int EPI = (2 * kFusedGridCap + 8) * 4;     // two segment lists and their counts
-    static constexpr int FIN = 4 * kFinItems * 32 * 16;          // finalize staging, per epilogue warp
+    static constexpr int FIN_ITEMS = NP == 32 ? 10 : 12;         // float4 rows (of 32 lanes) a finalizing warp stages
+    static constexpr int FIN = 4 * FIN_ITEMS * 32 * 16;          // finalize staging, all epilogue warps
     static constexpr int STAGES_RAW = (kSmemLimit - 1024 - CTRL - EPI - FIN) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int SMEM = 1024 + STAGES * STAGE + CTRL + EPI + FIN;
@@ -413,7 +413,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
     volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
     int* seg = reinterpret_cast<int*>(ctrl + C::CTRL);          // partial slots of the tile being finalized
-    float4* fin_buf = reinterpret_cast<float4*>(ctrl + C::CTRL + C::EPI);   // [4 warps][kFinItems][32 lanes]
+    float4* fin_buf = reinterpret_cast<float4*>(ctrl + C::CTRL + C::EPI);   // [4 warps][FIN_ITEMS][32 lanes]
     int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
     volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, jseg, nseg2, jseg2]
 
@@ -795,51 +795,83 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                 };
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
-                // A warp takes its tokens one at a time.  Each lane copies its
-                // own 16 bytes (4 rows) of every partial segment of the token
-                // (both planes for gate/up) into the warp's staging rows with
-                // cp.async, up to SB segments per batch, all in flight at
-                // once, and adds them from shared memory in k order; the
-                // residual, or the token's RMSNorm tile sums (lanes over the
-                // tiles, summed lane-strided then by a butterfly: a fixed
-                // order), load alongside.
-                const uint32_t fb_s = smem_addr(fin_buf + q * (kFinItems * 32) + lane);
-                const float4* fb = fin_buf + q * (kFinItems * 32) + lane;
-                auto share = [&](auto dual_c, auto norm_c) {
+                // A warp takes TB of its tokens at a time (TB = 2 when their
+                // segments fit its staging rows, else 1).  Each lane copies
+                // its own 16 bytes (4 rows) of every partial segment of the
+                // batch's tokens (both planes for gate/up) into the warp's
+                // staging rows with cp.async, up to SB segments per token and
+                // batch, all in flight at once, and adds them from shared
+                // memory in k order; the residuals, or the tokens' RMSNorm
+                // tile sums (lanes over the tiles, summed lane-strided then by
+                // a butterfly: a fixed order), load alongside.
+                const uint32_t fb_s = smem_addr(fin_buf + q * (C::FIN_ITEMS * 32) + lane);
+                const float4* fb = fin_buf + q * (C::FIN_ITEMS * 32) + lane;
+                auto share_tb = [&](auto tb_c, auto dual_c, auto norm_c) {
+                    constexpr int TB = decltype(tb_c)::value;
                     constexpr bool DU = decltype(dual_c)::value, NO = decltype(norm_c)::value;
                     constexpr int PL = DU ? 2 : 1;
-                    constexpr int SB = kFinItems / PL;
-                    for (int t = t_lo + q; t < t_hi; t += 4) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
-                        uint2 rv = make_uint2(0u, 0u);
-                        float ssq = 0.f;
-                        if (has_resid && r0 < D) rv = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
-                        if constexpr (NO) {
-                            for (int m2 = lane; m2 < Dt; m2 += 32) ssq += __ldcg(sl + m2 * B + t);
+                    constexpr int SB = C::FIN_ITEMS / (PL * TB);
+                    for (int t0 = t_lo + q; t0 < t_hi; t0 += 4 * TB) {
+                        float4 acc[TB], acc2[TB];
+                        uint2 rv[TB];
+                        float ssq[TB];
+#pragma unroll
+                        for (int j = 0; j < TB; ++j) {
+                            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            acc2[j] = acc[j];
+                            rv[j] = make_uint2(0u, 0u);
+                            ssq[j] = 0.f;
+                            const int t = t0 + 4 * j;
+                            if (t < t_hi) {
+                                if (has_resid && r0 < D)
+                                    rv[j] = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
+                                if constexpr (NO) {
+                                    for (int m2 = lane; m2 < Dt; m2 += 32) ssq[j] += __ldcg(sl + m2 * B + t);
+                                }
+                            }
                         }
                         for (int s0 = 0; s0 < nseg; s0 += SB) {
                             const int nb = min(SB, nseg - s0);
 #pragma unroll
-                            for (int k2 = 0; k2 < SB; ++k2) {
-                                if (k2 < nb) {
-                                    const float* sp = pbase + (size_t)slot_of(s0 + k2) * C::PART_FLOATS + t * 128;
-                                    cp_async16(fb_s + (uint32_t)(k2 * PL) * 512u, sp);
-                                    if constexpr (DU) cp_async16(fb_s + (uint32_t)(k2 * PL + 1) * 512u, sp + NP * 128);
+                            for (int j = 0; j < TB; ++j) {
+#pragma unroll
+                                for (int k2 = 0; k2 < SB; ++k2) {
+                                    const int t = t0 + 4 * j;
+                                    if (t < t_hi && k2 < nb) {
+                                        const float* sp = pbase + (size_t)slot_of(s0 + k2) * C::PART_FLOATS + t * 128;
+                                        const uint32_t it = (uint32_t)((j * SB + k2) * PL);
+                                        cp_async16(fb_s + it * 512u, sp);
+                                        if constexpr (DU) cp_async16(fb_s + (it + 1) * 512u, sp + NP * 128);
+                                    }
                                 }
                             }
                             cp_async_wait_all();
 #pragma unroll
-                            for (int k2 = 0; k2 < SB; ++k2) {
-                                if (k2 < nb) {
-                                    add4(acc, fb[(k2 * PL) * 32]);
-                                    if constexpr (DU) add4(acc2, fb[(k2 * PL + 1) * 32]);
+                            for (int j = 0; j < TB; ++j) {
+#pragma unroll
+                                for (int k2 = 0; k2 < SB; ++k2) {
+                                    if (t0 + 4 * j < t_hi && k2 < nb) {
+                                        const int it = (j * SB + k2) * PL;
+                                        add4(acc[j], fb[it * 32]);
+                                        if constexpr (DU) add4(acc2[j], fb[(it + 1) * 32]);
+                                    }
                                 }
                             }
                         }
-                        float sc = 1.f;
-                        if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq) / (float)D + p.eps);
-                        emit(t, acc, acc2, rv, sc);
+#pragma unroll
+                        for (int j = 0; j < TB; ++j) {
+                            float sc = 1.f;
+                            if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq[j]) / (float)D + p.eps);
+                            if (t0 + 4 * j < t_hi) emit(t0 + 4 * j, acc[j], acc2[j], rv[j], sc);
+                        }
                     }
+                };
+                using I1 = std::integral_constant<int, 1>;
+                using I2 = std::integral_constant<int, 2>;
+                auto share = [&](auto dual_c, auto norm_c) {
+                    constexpr int PL = decltype(dual_c)::value ? 2 : 1;
+                    if (NP > 32 && 2 * PL * nseg <= C::FIN_ITEMS) share_tb(I2{}, dual_c, norm_c);
+                    else share_tb(I1{}, dual_c, norm_c);
                 };
                 using T = std::true_type;
                 using Fa = std::false_type;
