@@ -415,7 +415,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     int* seg = reinterpret_cast<int*>(ctrl + C::CTRL);          // partial slots of the tile being finalized
     float4* fin_buf = reinterpret_cast<float4*>(ctrl + C::CTRL + C::EPI);   // [4 warps][FIN_ITEMS][32 lanes]
     int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
-    volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, jseg, nseg2, jseg2]
+    volatile int* seg_info = seg2 + kFusedGridCap;              // [nseg, -, nseg2, -]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, cta = blockIdx.x;
@@ -681,10 +681,13 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (leader && !dead && !skip) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
             }
             if (p.parallel && ph.kind == K_OPROJ) continue;    // finalized with down
-            // pass 2: once all of a tile's units have arrived (a tile ticket
-            // counts arrivals monotonically over the layers of the launch),
-            // the CTAs holding them (contiguous, skipping CTAs without work)
-            // each finalize a share of the tile's tokens
+            // pass 2: the phase's (tile, token) pairs, m_tiles x B in
+            // tile-major order, are split evenly over the CTAs; CTA c
+            // finalizes pairs [c W / G, (c+1) W / G), a tile at a time, once
+            // all of the tile's units have arrived (a tile ticket counts
+            // arrivals monotonically over the layers of the launch).  Any CTA
+            // can finalize any tile: its partials are added in k order, so the
+            // sum does not depend on which CTA adds them.
             // segments of tile mt of phase phx in k order: the CTAs from the
             // owner of its first k-block to the owner of its last one, all of
             // which hold work unless the phase has fewer pairs than CTAs (then
@@ -694,16 +697,15 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 cf_ = owner_of((int64_t)mt_ * phx.nkb, phx.total, G);
                 const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1, phx.total, G);
                 if (!every_ && warp == 2) {
-                    int n = 0, j = 0;
+                    int n = 0;
                     for (int base = cf_; base <= cl_; base += 32) {
                         const int cc = base + lane;
                         const bool w = cc <= cl_ && has_work(phx.total, G, cc);
                         const unsigned m = __ballot_sync(0xFFFFFFFFu, w);
                         if (w) list[n + __popc(m & ((1u << lane) - 1u))] = cc + mt_;
                         n += __popc(m);
-                        j += __popc(__ballot_sync(0xFFFFFFFFu, w && cc < cta));
                     }
-                    if (lane == 0) { seg_info[info] = n; seg_info[info + 1] = j; }
+                    if (lane == 0) seg_info[info] = n;
                 }
                 return cl_;
             };
@@ -712,8 +714,14 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // the serial block's MLP normalises h, everything else the layer input
             const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
             bool prev_done = ph.prev_fin < 0;
-            Units u2(ph, G, cta);
-            while (u2.next(mt, kb0, kb1)) {
+            const int64_t npairs = (int64_t)ph.m_tiles * B;
+            const int64_t f1 = npairs * (cta + 1) / G;
+            for (int64_t f = npairs * cta / G; f < f1;) {
+                mt = (int)(f / B);
+                // this CTA's tokens of tile mt
+                const int t_lo = (int)(f - (int64_t)mt * B);
+                const int t_hi = (int)min((int64_t)B, f1 - (int64_t)mt * B);
+                f = (int64_t)mt * B + t_hi;
                 int cf, cf_o = 0;
                 bool every, every_o = true;
                 const int cl = seg_list(ph, mt, seg, 0, cf, every);
@@ -721,7 +729,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (merged) cl_o = seg_list(ph_o, mt, seg2, 2, cf_o, every_o);
                 epi_sync();
                 const int nseg_d = every ? cl - cf + 1 : seg_info[0];
-                const int jseg = every ? cta - cf : seg_info[1];
                 const int nseg_o = !merged ? 0 : (every_o ? cl_o - cf_o + 1 : seg_info[2]);
                 const int nseg = nseg_o + nseg_d;
                 // slot of segment j: the o_proj segments first, then this
@@ -732,10 +739,6 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     return (size_t)ph.kind * region + (size_t)(every ? cf + jd + mt : seg[jd]);
                 };
 
-                // this CTA's share of the tile's tokens (none for most CTAs
-                // when B is small: those do not wait for the tile)
-                const int t_lo = (int)((int64_t)B * jseg / nseg_d), t_hi = (int)((int64_t)B * (jseg + 1) / nseg_d);
-                if (t_lo == t_hi) { epi_sync(); continue; }
                 // every unit of the tile has arrived, and the phase finalized
                 // before this one is complete (so are all earlier ones: each
                 // waited likewise); two threads wait side by side
