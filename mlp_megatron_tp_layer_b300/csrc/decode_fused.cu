@@ -13,7 +13,9 @@
 // operand (padded to NP by TMA's zero fill), accumulators in TMEM.
 //
 // Work split: a phase's work is the flattened list of (m-tile, 64-wide
-// k-block) pairs; CTA c of G takes the contiguous range [c T/G, (c+1) T/G).
+// k-block) pairs; CTA c of g takes the contiguous range [c T/g, (c+1) T/g),
+// with g = m_tiles x s (every tile exactly s segments) when that still uses
+// at least 94% of the G CTAs, else g = G.
 // A range may cover parts of several m-tiles ("units"); each unit leaves an
 // fp32 partial tile in global memory and counts itself on the tile's ticket.
 // Once all of a tile's units have arrived, the CTAs that hold them each
@@ -119,6 +121,7 @@ struct FCfg {
 
 struct Phase {
     int kind, layer, m_tiles, nkb, M;
+    int gw;                    // CTAs holding units of the phase: 0 .. gw-1
     int prev_fin;              // phase whose completion this phase's finalize waits for (-1: none)
     int src_kind;              // kind whose output tiles the activation loads wait for (-1: launch input)
     unsigned src_target;       // ready count of such a tile once this layer's input is final
@@ -176,6 +179,12 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     ph.m_tiles = (ph.M + 127) / 128;
     ph.nkb = (K + 63) / 64;
     ph.total = (int64_t)ph.m_tiles * ph.nkb;
+    // every tile split into exactly s segments when m_tiles x s CTAs still
+    // cover at least 94% of the grid (fewer, aligned segments: less partial
+    // traffic per tile; the CTAs left over stream no weights in this phase)
+    ph.gw = p.G;
+    const int s = min(p.G / ph.m_tiles, ph.nkb);
+    if (s >= 1 && ph.m_tiles * s * 100 >= p.G * 94) ph.gw = ph.m_tiles * s;
     return ph;
 }
 
@@ -239,8 +248,9 @@ struct Units {
     int64_t idx, hi;
     int nkb;
     __device__ __forceinline__ Units() : idx(0), hi(0), nkb(1) {}
-    __device__ __forceinline__ Units(const Phase& ph, int G, int c)
-        : idx(ph.total * c / G), hi(ph.total * (c + 1) / G), nkb(ph.nkb) {}
+    __device__ __forceinline__ Units(const Phase& ph, int c)
+        : idx(c < ph.gw ? ph.total * c / ph.gw : 0), hi(c < ph.gw ? ph.total * (c + 1) / ph.gw : 0),
+          nkb(ph.nkb) {}
     __device__ __forceinline__ bool next(int& mt, int& kb0, int& kb1) {
         if (idx >= hi) return false;
         mt = (int)(idx / nkb);
@@ -272,7 +282,7 @@ struct TileCursor {
             if (k >= 1 && u.next(mt, kb0, kb1)) { kb = kb0; hf = 0; continue; }
             if (++k >= n_phases) return false;
             ph = phase_of(mp, p, k);
-            u = Units(ph, G, cta);
+            u = Units(ph, cta);
             kb = kb1 = 0;
         }
     }
@@ -499,7 +509,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         for (int k = 1; k < n_phases && ok; ++k) {
             const Phase ph = phase_of(mp, p, k);
             const int halves = ph.kind == K_GATEUP ? 2 : 1;
-            const Units u(ph, G, cta);            // this CTA's pairs [u.idx, u.hi), in k order per m-tile
+            const Units u(ph, cta);            // this CTA's pairs [u.idx, u.hi), in k order per m-tile
             for (int64_t idx = u.idx; ok && idx < u.hi;) {
                 int n = (int)min(u.hi - idx, (int64_t)32);
                 if (ph.src_kind >= 0) {
@@ -549,7 +559,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             for (int k = 1; k < n_phases && ok; ++k) {
                 const Phase ph = phase_of(mp, p, k);
                 const bool dual = ph.kind == K_GATEUP;
-                Units u(ph, G, cta);
+                Units u(ph, cta);
                 int mt, kb0, kb1;
                 while (ok && u.next(mt, kb0, kb1)) {
                     const int a = uc & 1;
@@ -645,7 +655,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // down tile's ticket and its finalize
             const bool merged = p.parallel && ph.kind == K_DOWN;
             const int tk_kind = (p.parallel && ph.kind == K_OPROJ) ? K_DOWN : ph.kind;
-            Units u(ph, G, cta);
+            Units u(ph, cta);
             int mt, kb0, kb1;
             const int first_uc = uc;
             // pass 1: drain every unit into its partial slot and count it on
@@ -693,14 +703,14 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // which hold work unless the phase has fewer pairs than CTAs (then
             // warp 2 lists the ones that do into list / seg_info[info])
             auto seg_list = [&](const Phase& phx, int mt_, int* list, int info, int& cf_, bool& every_) {
-                every_ = phx.total >= G;
-                cf_ = owner_of((int64_t)mt_ * phx.nkb, phx.total, G);
-                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1, phx.total, G);
+                every_ = phx.total >= phx.gw;
+                cf_ = owner_of((int64_t)mt_ * phx.nkb, phx.total, phx.gw);
+                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1, phx.total, phx.gw);
                 if (!every_ && warp == 2) {
                     int n = 0;
                     for (int base = cf_; base <= cl_; base += 32) {
                         const int cc = base + lane;
-                        const bool w = cc <= cl_ && has_work(phx.total, G, cc);
+                        const bool w = cc <= cl_ && has_work(phx.total, phx.gw, cc);
                         const unsigned m = __ballot_sync(0xFFFFFFFFu, w);
                         if (w) list[n + __popc(m & ((1u << lane) - 1u))] = cc + mt_;
                         n += __popc(m);

@@ -33,9 +33,23 @@ def _needs_gpu():
     assert tpl.device_status() == 0
 
 
-# D 1024, F 2048: gate/up and down have 256 (m-tile, k-block) pairs, so every
-# one of the 148 CTAs holds work there; the last CTA holds work in every phase.
 SHAPE = dict(D=1024, F=2048, n_q=8, n_kv=2, hd=128, tp=2, L=2)
+GRID = 148
+
+
+def last_cta_with_work(M, K, G=GRID):
+    """The fused stack gives a projection of M output rows and depth K to
+    g = m_tiles x s CTAs (every 128-row tile split into s k-ranges) when that
+    still covers 94% of the G CTAs, else to all G; the last of them always
+    holds the phase's last (m-tile, k-block) pair."""
+    m_tiles, nkb = -(-M // 128), -(-K // 64)
+    s = min(G // m_tiles, nkb)
+    g = m_tiles * s if s >= 1 and m_tiles * s * 100 >= G * 94 else G
+    return g - 1
+
+
+_S = SHAPE
+_QKV_ROWS = (_S["n_q"] + 2 * _S["n_kv"]) * _S["hd"]
 
 
 def _stack(B, block):
@@ -52,10 +66,10 @@ def _stack(B, block):
 
 # (cta, phase): phase 4 l + 1 + j is projection j of layer l in the block's order
 @pytest.mark.parametrize("B,block,cta,phase", [
-    (1, tpl.BLOCK_SERIAL, 147, 1),       # QKV of layer 0
-    (40, tpl.BLOCK_SERIAL, 0, 3),        # gate/up of layer 0
-    (1, tpl.BLOCK_SERIAL, 147, 8),       # down of layer 1
-    (16, tpl.BLOCK_PARALLEL, 147, 3),    # o_proj, finalized together with down
+    (1, tpl.BLOCK_SERIAL, last_cta_with_work(_QKV_ROWS, _S["D"]), 1),                  # QKV of layer 0
+    (40, tpl.BLOCK_SERIAL, 0, 3),                                                       # gate/up of layer 0
+    (1, tpl.BLOCK_SERIAL, last_cta_with_work(_S["D"], _S["F"]), 8),                     # down of layer 1
+    (16, tpl.BLOCK_PARALLEL, last_cta_with_work(_S["D"], _S["n_q"] * _S["hd"]), 3),     # o_proj, finalized with down
 ])
 def test_fused_stack_wait_runs_out_and_the_next_call_is_clean(B, block, cta, phase):
     run = _stack(B, block)
