@@ -169,7 +169,7 @@ KSplit rowpar_split(int dt, int64_t tokens, int64_t out_features, int64_t K, int
 // epilogue; W1 is the second weight for SwiGLU.  Chooses the kernel by tokens.
 cudaError_t project(const char* tag, int dt, const void* X, int64_t ldx, int64_t tokens, const void* W,
                     const void* W1, int64_t ldw, int64_t features, int64_t K, const KSplit& ks, const Epilogue& epi,
-                    cudaStream_t st) {
+                    cudaStream_t st, float* tail_ws = nullptr, size_t tail_ws_bytes = 0) {
     Path p = pick_path(dt, tokens);
     if (p != PATH_SIMT && !tc_split_ok(ks)) p = PATH_SIMT;
     if (p == PATH_SIMT) {
@@ -196,6 +196,8 @@ cudaError_t project(const char* tag, int dt, const void* X, int64_t ldx, int64_t
     g.K = K;
     g.ks = ks;
     g.epi = epi;
+    g.tail_ws = tail_ws;
+    g.tail_ws_bytes = tail_ws_bytes;
     if (p == PATH_TC_SWAP) {
         g.swap = true;
         g.A = W; g.A2 = W1; g.lda = ldw; g.M = features;
@@ -574,14 +576,15 @@ CasePlan plan_case(int case_id, int64_t I, int64_t J, int64_t K, int X, int dt, 
     CasePlan c{};
     c.ks = whole(J);
     c.partial_path = false;
-    c.total = 0;
+    // the direct GEMM's split last wave (the same shape rule the launch applies)
+    c.total = pick_path(dt, I) == PATH_TC ? up(tc_tail_ws_bytes(I, K, J, kDesignSMs)) : 0;
     if (case_id == 3) {
         const Path path = pick_path(dt, I);
         if (want_partials || path != PATH_TC) {
             c.partial_path = true;
+            c.total = 0;
             if (want_partials && path == PATH_TC && (J / X) % 64 == 0) {
                 c.ks.tp = X; c.ks.sub = 1; c.ks.k_shard = J / X; c.ks.k_chunk = J / X;
-                c.total = 0;
             } else {
                 c.ks = rowpar_split(dt, I, K, J, X);
                 c.total = up((size_t)c.ks.tp * c.ks.sub * I * K * 4);
@@ -667,7 +670,8 @@ extern "C" tpl_status tpl_sharded_matmul(int case_id, int mode, int gather, cons
         // cases 1, 2, 4: the gathered operand is a view of the shards already
         // resident in this GPU's memory; case 3 fused: partial sums over the J
         // shards accumulate in ascending shard order inside the GEMM.
-        err = project("matmul", dtype, A, J, I, Bt, nullptr, J, K, J, whole(J), e, st);
+        err = project("matmul", dtype, A, J, I, Bt, nullptr, J, K, J, whole(J), e, st, reinterpret_cast<float*>(ws),
+                      ws ? ws_bytes : 0);
         return cuda_status(err);
     }
     float* part = partials;

@@ -150,8 +150,14 @@ struct TcGemmArgs {
     KSplit ks;
     bool swap;
     Epilogue epi;
+    float* tail_ws;          // scratch for the split last wave (tc_tail_ws_bytes), or null
+    size_t tail_ws_bytes;
 };
 bool tc_gemm_supported();
+// A plain-store GEMM (normal orientation, one split) whose tiles leave a
+// partial last wave splits the tiles of that wave along K over all CTAs; the
+// chunks' fp32 partials need this much scratch (0: no split for this shape).
+size_t tc_tail_ws_bytes(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st);
 
 // TMA descriptor of a bf16 matrix [rows, cols] (row pitch ld elements), box

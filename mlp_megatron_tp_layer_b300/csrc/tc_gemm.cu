@@ -45,6 +45,13 @@ struct TcParams {
     KSplit ks;
     Epilogue epi;
     unsigned int* err;
+    // split last wave: tiles [main_tiles, total_tiles) are cut into tail_s
+    // K-chunks each; CTA b < tail tiles x tail_s computes chunk b % tail_s of
+    // tail tile b / tail_s after its whole tiles and writes an fp32 partial
+    // (column-major [OUT_COLS][BM]) to slot b of tail_ws
+    int64_t main_tiles;
+    int tail_s;
+    float* tail_ws;
 };
 
 template <int BN, bool SWAP, bool DUAL>
@@ -80,6 +87,32 @@ __device__ __forceinline__ void split_range(const TcParams& p, int sp, int64_t& 
     k0 = sh * p.ks.k_shard + (int64_t)j * p.ks.k_chunk;
     const int64_t k1 = min(k0 + p.ks.k_chunk, (int64_t)(sh + 1) * p.ks.k_shard);
     nkb = (int)((k1 - k0 + BK - 1) / BK);
+}
+
+// Work item `it` of this CTA: its whole tiles (blockIdx.x, + gridDim.x, ...)
+// below main_tiles, then at most one K-chunk of a tail tile.  slot < 0: a
+// whole tile; else the chunk's partial slot.
+struct Item { TileCoord c; int64_t k0; int nkb; int slot; };
+__device__ __forceinline__ bool item_of(const TcParams& p, int it, Item& w) {
+    const int b = blockIdx.x;
+    const int64_t n_main = p.main_tiles > b ? (p.main_tiles - 1 - b) / gridDim.x + 1 : 0;
+    if (it < n_main) {
+        w.c = tile_coord(p, b + (int64_t)it * gridDim.x);
+        split_range(p, w.c.sp, w.k0, w.nkb);
+        w.slot = -1;
+        return true;
+    }
+    if (it > n_main || p.tail_s == 0 || b >= (p.total_tiles - p.main_tiles) * p.tail_s) return false;
+    const int i = b / p.tail_s, j = b - i * p.tail_s;
+    w.c = tile_coord(p, p.main_tiles + i);
+    int64_t k0;
+    int nkb;
+    split_range(p, w.c.sp, k0, nkb);
+    const int kb0 = (int)((int64_t)nkb * j / p.tail_s), kb1 = (int)((int64_t)nkb * (j + 1) / p.tail_s);
+    w.k0 = k0 + (int64_t)kb0 * BK;
+    w.nkb = kb1 - kb0;
+    w.slot = b;
+    return true;
 }
 
 template <int BN, bool SWAP, bool DUAL>
@@ -142,11 +175,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             int issued_tail = 0;   // stages loaded but not yet known to be consumed (abort drain)
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-                const TileCoord c = tile_coord(p, t);
-                int64_t k0;
-                int nkb;
-                split_range(p, c.sp, k0, nkb);
+            Item w;
+            for (int it = 0; ok && item_of(p, it, w); ++it) {
+                const TileCoord c = w.c;
+                const int64_t k0 = w.k0;
+                const int nkb = w.nkb;
                 const int am = c.mt * BM;
                 const int bn = c.nt * C::B_ROWS;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -186,12 +219,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int it = 0;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
-                const TileCoord c = tile_coord(p, t);
-                int64_t k0;
-                int nkb;
-                split_range(p, c.sp, k0, nkb);
+            Item w;
+            for (int it = 0; ok && item_of(p, it, w); ++it) {
+                const int nkb = w.nkb;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(smem_addr(&acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
@@ -227,9 +257,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        int it = 0;
-        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-            const TileCoord c = tile_coord(p, t);
+        Item w;
+        for (int it = 0; item_of(p, it, w); ++it) {
+            const TileCoord c = w.c;
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             // every lane polls; the vote keeps the warp converged for the
@@ -248,7 +278,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const int up_off = SWAP ? BN : BN / 2;
                     if (CH == 32) tmem_ld32(tbase + up_off + c0, u); else tmem_ld16(tbase + up_off + c0, u);
                 }
-                if (a_row < p.M) {
+                if (w.slot >= 0) {
+                    // tail chunk: the whole fp32 tile, column-major (lanes = rows: coalesced)
+                    float* dst = p.tail_ws + (size_t)w.slot * C::OUT_COLS * BM + row;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) dst[(size_t)(c0 + j) * BM] = v[j];
+                } else if (a_row < p.M) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
                         const int64_t b_row = (int64_t)c.nt * C::OUT_COLS + c0 + j;
@@ -274,6 +309,46 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+}
+
+// Tail tiles of a split last wave: element (row, col) of tail tile i is the
+// sum of its tail_s chunk partials in ascending k order (a fixed order), then
+// stored through the launch's epilogue.  Column-major within a tile, so the
+// threads of a warp read consecutive rows.
+template <int OUT_COLS>
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const TcParams p) {
+    const int64_t per = (int64_t)OUT_COLS * BM;
+    const int64_t n = (p.total_tiles - p.main_tiles) * per;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n; g += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(g / per);
+        const int64_t e = g - (int64_t)i * per;
+        const int col = (int)(e / BM), row = (int)(e - (int64_t)col * BM);
+        const float* src = p.tail_ws + (size_t)i * p.tail_s * per + e;
+        float v = 0.f;
+#pragma unroll 8
+        for (int j = 0; j < p.tail_s; ++j) v += __ldcs(src + (size_t)j * per);
+        const TileCoord c = tile_coord(p, p.main_tiles + i);
+        const int64_t tok = (int64_t)c.mt * BM + row, feat = (int64_t)c.nt * OUT_COLS + col;
+        if (tok < p.M && feat < p.NB) store_value(p.epi, 0, tok, feat, v);
+    }
+}
+
+// Split of the last wave (see TcParams): tail tiles and chunks per tile, for
+// a plain-store GEMM of M x N output with N-tiles of 256 and K-depth K.
+struct TailPlan { int64_t tail_tiles; int s; size_t bytes; };
+TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sms) {
+    TailPlan t{0, 0, 0};
+    const int64_t total = ((M + BM - 1) / BM) * ((N + 255) / 256);
+    const int64_t nkb = (K + BK - 1) / BK;
+    if (sms <= 0 || total <= sms || total >= 8LL * sms) return t;   // one partial wave, or a negligible tail
+    const int64_t tail = total % sms;
+    if (tail == 0) return t;
+    const int64_t s = std::min<int64_t>(sms / tail, nkb);
+    if (s < 2) return t;
+    t.tail_tiles = tail;
+    t.s = (int)s;
+    t.bytes = (size_t)tail * s * 256 * BM * 4;
+    return t;
 }
 
 // ---------------------------------------------------------------- host side
@@ -366,12 +441,30 @@ cudaError_t launch_cfg(const TcGemmArgs& a, cudaStream_t st) {
     p.ks = a.ks;
     p.epi = a.epi;
     p.err = ctx->err_word;
+    p.main_tiles = p.total_tiles;
+    p.tail_s = 0;
+    p.tail_ws = nullptr;
+    if (!SWAP && !DUAL && C::OUT_COLS == 256 && a.epi.mode == EPI_STORE && p.splits == 1 && a.tail_ws) {
+        const TailPlan t = tail_plan(a.M, a.N, a.K, ctx->num_sms);
+        if (t.s > 0 && t.bytes <= a.tail_ws_bytes) {
+            p.main_tiles = p.total_tiles - t.tail_tiles;
+            p.tail_s = t.s;
+            p.tail_ws = a.tail_ws;
+        }
+    }
     const int64_t grid = std::min<int64_t>(p.total_tiles, ctx->num_sms);
     tc_gemm_kernel<BN, SWAP, DUAL><<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(mA, mA2, mB, mB2, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.tail_s == 0) return e;
+    const int64_t n = (p.total_tiles - p.main_tiles) * C::OUT_COLS * BM;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)ctx->num_sms * 8);
+    tail_reduce_kernel<C::OUT_COLS><<<blocks, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t tc_tail_ws_bytes(int64_t M, int64_t N, int64_t K, int sms) { return tail_plan(M, N, K, sms).bytes; }
 
 bool tma_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
     return cached_map(m, base, rows, cols, ld, box_rows);

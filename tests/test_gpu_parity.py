@@ -179,6 +179,30 @@ def test_sharded_matmul_layout_bit_exact(I, case, mode, gather):
     assert_equal(C, C_ref, what="C")
 
 
+# 2 x 80 output tiles of 128 x 256 = 160 tiles on 148 SMs: the GEMM runs one
+# full wave and splits the 12 tiles of its last wave along K (8 chunks each),
+# then sums each tile's chunk partials in k order
+@pytest.mark.parametrize("case,mode,gather", CASES)
+def test_sharded_matmul_split_last_wave(case, mode, gather):
+    I, J, K, X = 256, 512, 20480, 4
+    if torch.cuda.get_device_properties(0).multi_processor_count == 148:
+        assert tpl.case_workspace_bytes(case, mode, I, J, K, X) > 0 or case == 3
+    A = si.normal((I, J), 1.0, 3, "cw.A", device="cuda")
+    Bt = si.normal((K, J), 1.0 / np.sqrt(J), 3, "cw.Bt", device="cuda")
+    C_ref, _ = _oracle_case(case, mode, gather, to_np(A), to_np(Bt), X, bf16=False)
+    C32 = tpl.sharded_matmul(case, A, Bt, X, mode, gather, out_dtype=torch.float32)
+    assert_close(C32, C_ref, what="C fp32")
+    Cb = tpl.sharded_matmul(case, A, Bt, X, mode, gather)
+    assert_close(Cb, C_ref, bf16_out=True, what="C bf16")
+    # integer data: every order of the sums is exact, so the layout is checked bit for bit
+    Ai = si.small_integers((I, J), 4, "cwi.A", -2, 2, device="cuda")
+    Bi = si.small_integers((K, J), 4, "cwi.Bt", -1, 1, device="cuda", zero_frac_num=8)
+    C_int, _ = _oracle_case(case, mode, gather, to_np(Ai), to_np(Bi), X, bf16=True)
+    assert_equal(tpl.sharded_matmul(case, Ai, Bi, X, mode, gather), C_int, what="C integer data")
+    # deterministic: a second call gives the same bits
+    assert torch.equal(tpl.sharded_matmul(case, A, Bt, X, mode, gather, out_dtype=torch.float32), C32)
+
+
 # ------------------------------------------------------ shard_reduce
 
 @pytest.mark.parametrize("tp", [1, 2, 3, 8])
