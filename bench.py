@@ -74,7 +74,12 @@ def args_parse():
     ap.add_argument("--only", choices=["decode", "prefill", "llama", "lm_head", "w8", "cases"], default=None,
                     help="run one workload only (small cases for profiling); prints that workload's line")
     ap.add_argument("--batches", type=str, default=None, help="decode batch sizes, comma-separated")
+    ap.add_argument("--phase-trace", action="store_true",
+                    help="per-phase timeline of the fused decode stack from the instrumented library "
+                         "(build it with: python mlp_megatron_tp_layer_b300/build.py --trace); with "
+                         "--model, --batches and --layers; prints one JSON line per batch size")
     ap.add_argument("--prefill-tokens", type=int, default=LP["B"])
+    ap.add_argument("--block", choices=["serial", "parallel"], default="serial", help="with --phase-trace")
     return ap.parse_args()
 
 
@@ -800,8 +805,60 @@ def run_prefill(args, tpl, dev, world, peaks, peak_kind, stream):
     return prefill
 
 
+TRACE_EVENTS = ("act_ready", "mma_start", "first_ticket", "drained", "fin_start", "published", "w_first",
+                "act_wait")
+
+
+def run_phase_trace(args):
+    """Per-phase event times of one fused-stack launch (instrumented library):
+    for every phase, the median and the maximum over CTAs of each event, in us
+    from the launch's first stamp.  Not a benchmark number: the stamps add a
+    few stores per phase."""
+    os.environ["TPL_LIBRARY"] = os.path.join(ROOT, "mlp_megatron_tp_layer_b300", "libtpl_trace.so")
+    import numpy as np
+    import mlp_megatron_tp_layer_b300 as tpl
+    model = args.model or "qwen2.5-1.5b"
+    cfg = QW if model.startswith("qwen") else LD
+    D, F, n_q, n_kv, hd, tp = cfg["D"], cfg["F"], cfg["n_q"], cfg["n_kv"], cfg["head_dim"], cfg["tp"]
+    L = min(args.layers, 4) if model.startswith("qwen") else min(args.llama_layers, 2)
+    block = tpl.BLOCK_PARALLEL if args.block == "parallel" else tpl.BLOCK_SERIAL
+    prefix = "qwen" if model.startswith("qwen") else "llama"
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=0, layer=l, prefix=prefix, device="cuda") for l in range(L)]
+    batches = [int(b) for b in args.batches.split(",")] if args.batches else list(cfg["batches"])
+    kinds = ["QKV", "GATEUP", "OPROJ", "DOWN"] if block == tpl.BLOCK_PARALLEL else ["QKV", "OPROJ", "GATEUP", "DOWN"]
+    for B in batches:
+        x = si.activations(B, D, seed=1, name=f"bench.x{B}", device="cuda")
+        for _ in range(3):
+            y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, block=block, path=tpl.PATH_FUSED)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, block=block, path=tpl.PATH_FUSED)
+        b.record()
+        torch.cuda.synchronize()
+        tr = tpl.fused_trace().astype(np.float64)
+        t0 = tr[tr > 0].min()
+        tr = np.where(tr > 0, (tr - t0) / 1e3, np.nan)
+        phases = []
+        for k in range(1, 4 * L + 1):
+            row = {"phase": k, "layer": (k - 1) // 4, "kind": kinds[(k - 1) % 4]}
+            for e, name in enumerate(TRACE_EVENTS):
+                v = tr[:, k, e]
+                v = v[~np.isnan(v)]
+                if v.size:
+                    row[name] = [round(float(np.median(v)), 2), round(float(v.max()), 2)]
+            phases.append(row)
+        print(json.dumps({"phase_trace": model, "block": args.block, "B": B, "layers": L,
+                          "launch_us": round(a.elapsed_time(b) * 1e3, 1), "events": "[median, max] us over CTAs",
+                          "phases": phases}), flush=True)
+        del y
+
+
 def main():
     args = args_parse()
+    if args.phase_trace:
+        run_phase_trace(args)
+        return
     rank, world = dist_init()
     if args.impl == "reference":
         run_reference(args, rank, world)

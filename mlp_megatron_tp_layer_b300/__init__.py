@@ -17,7 +17,9 @@ import re
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtpl.so")
+# TPL_LIBRARY selects another build of the same library, e.g. the instrumented
+# libtpl_trace.so (build.py --trace) for phase traces.
+LIB_PATH = os.environ.get("TPL_LIBRARY") or os.path.join(_HERE, "libtpl.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "tpl.h")
 
 F32, BF16 = 0, 1
@@ -51,6 +53,7 @@ _SIGS = {
     "tpl_profile_count": (_i32, []),
     "tpl_profile_read": (_i32, [_i32, ctypes.c_char_p, _sz, ctypes.POINTER(ctypes.c_float)]),
     "tpl_test_fused_fault": (_i32, [_i32, _i32, _i64]),
+    "tpl_fused_trace_read": (_i32, [_vp, _sz]),
     "tpl_tp_decoder_workspace": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tpl_tp_decoder_stack_path": (_i32, [_vp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _i64, _i64, _i64, _i32,
@@ -420,6 +423,18 @@ def test_fused_fault(cta: int = -1, phase: int = 1, wait_limit_ns: int = 0):
     launches leave out its first ticket arrival of `phase`, with every wait
     limited to wait_limit_ns; test_fused_fault() restores the defaults."""
     _check(lib.tpl_test_fused_fault(cta, phase, wait_limit_ns), "tpl_test_fused_fault")
+
+
+FUSED_TRACE_SHAPE = (148, 129, 8)    # CTAs, phases, events (see tpl_fused_trace_read)
+
+
+def fused_trace():
+    """Per-CTA, per-phase event stamps (ns) of the last fused-stack launch of an
+    instrumented build, as an int64 array FUSED_TRACE_SHAPE (0: not reached)."""
+    import numpy as np
+    buf = np.zeros(FUSED_TRACE_SHAPE, dtype=np.uint64)
+    _check(lib.tpl_fused_trace_read(ctypes.c_void_p(buf.ctypes.data), buf.nbytes), "tpl_fused_trace_read")
+    return buf.astype(np.int64)
 
 
 def profile_enable(max_launches: int = 4096):

@@ -40,10 +40,11 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(p) > t for p in [src] + HEADERS)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, verbose: bool, build_dir: str = BUILD, defines=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-           "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+           "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), *[f"-D{d}" for d in defines],
+           "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -54,28 +55,35 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Build libtpl.so; with trace, the instrumented libtpl_trace.so (fused-stack
+    phase stamps, read with tpl_fused_trace_read) from objects of its own."""
+    build_dir = BUILD + "_trace" if trace else BUILD
+    lib = os.path.join(HERE, "libtpl_trace.so") if trace else LIB
+    defines = ("TPL_FUSED_TRACE",) if trace else ()
+    os.makedirs(build_dir, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
+    objs = [os.path.join(build_dir, os.path.basename(s) + ".o") for s in srcs]
     todo = [s for s, o in zip(srcs, objs) if force or _stale(o, s)]
     if todo:
         with cf.ThreadPoolExecutor(max_workers=len(todo)) as ex:
-            list(ex.map(lambda s: _compile(s, verbose), todo))
-    if todo or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
+            list(ex.map(lambda s: _compile(s, verbose, build_dir, defines), todo))
+    if todo or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        LIBOUT = lib
+        tmp = LIBOUT + ".tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIBOUT)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--trace", action="store_true", help="the instrumented libtpl_trace.so")
     a = ap.parse_args()
-    print(build(a.force, a.verbose))
+    print(build(a.force, a.verbose, a.trace))

@@ -751,6 +751,13 @@ extern "C" tpl_status tpl_tp_decoder_stack_ex(const void* x, void* y, const void
     return TPL_OK;
 }
 
+extern "C" tpl_status tpl_fused_trace_read(void* host, size_t bytes) {
+    if (!host) return TPL_ERR_NULL;
+    if (!device_ctx()) return TPL_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TPL_ERR_CUDA;
+    return fused_trace_read(host, bytes) ? TPL_OK : TPL_ERR_UNSUPPORTED;
+}
+
 extern "C" tpl_status tpl_test_fused_fault(int cta, int phase, int64_t wait_limit_ns) {
     if (wait_limit_ns > 2000000000LL) return TPL_ERR_UNSUPPORTED;
     if (wait_limit_ns > 0 && wait_limit_ns < 10000) return TPL_ERR_UNSUPPORTED;

@@ -61,6 +61,19 @@
 #include "ptx.cuh"
 
 namespace tpl {
+
+// Phase trace (instrumented builds only, -DTPL_FUSED_TRACE): per CTA and
+// phase of the last launch, %globaltimer stamps of kFusedTraceEvents events
+// (see tpl_fused_trace_read).  In normal builds the stamps compile to nothing.
+#ifdef TPL_FUSED_TRACE
+constexpr int kFusedTracePhases = 1 + 4 * kFusedMaxLayers;
+__device__ unsigned long long g_fused_trace[kFusedGridCap * kFusedTracePhases * kFusedTraceEvents];
+#define TPL_TRACE(k, e) \
+    (g_fused_trace[((size_t)cta * kFusedTracePhases + (k)) * kFusedTraceEvents + (e)] = globaltimer())
+#else
+#define TPL_TRACE(k, e) ((void)0)
+#endif
+
 namespace {
 
 constexpr int kFThreads = 224;
@@ -473,7 +486,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const CUtensorMap* map;
             int x, y;
             bool ok = true;
+            int traced_k = -1;
             while (ok && ld.next(mp, p, G, cta, n_phases, map, x, y)) {
+                if (ld.k != traced_k) { traced_k = ld.k; TPL_TRACE(ld.k, 6); }
                 if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
                 const uint32_t fb = smem_addr(&full_w[stage]);
                 mbar_expect_tx(fb, C::W_BYTES);
@@ -512,10 +527,13 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const Units u(ph, cta);            // this CTA's pairs [u.idx, u.hi), in k order per m-tile
             for (int64_t idx = u.idx; ok && idx < u.hi;) {
                 int n = (int)min(u.hi - idx, (int64_t)32);
+                const bool first_k = idx == u.idx;
+                if (first_k && lane == 0) TPL_TRACE(k, 7);
                 if (ph.src_kind >= 0) {
                     n = ready_prefix(p, ph, idx, u.hi, lane, labort, gabort);
                     if (n == 0) { ok = false; break; }
                 }
+                if (first_k && lane == 0) TPL_TRACE(k, 0);
                 if (lane == 0) {
                     for (int j = 0; j < n && ok; ++j) {
                         const int kb = (int)((idx + j) % ph.nkb);
@@ -561,6 +579,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const bool dual = ph.kind == K_GATEUP;
                 Units u(ph, cta);
                 int mt, kb0, kb1;
+                const int uc_phase0 = uc;
                 while (ok && u.next(mt, kb0, kb1)) {
                     const int a = uc & 1;
                     if (!mbar_wait(smem_addr(&acc_empty[a]), ((uc >> 1) & 1) ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
@@ -570,6 +589,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                         if (!mbar_wait(smem_addr(&full_w[stage]), par, labort, gabort, p.wait_ns) ||
                             !mbar_wait(smem_addr(&full_x[stage]), par, labort, gabort, p.wait_ns)) { ok = false; break; }
                         tc_fence_after();
+                        if (kb == kb0 && uc == uc_phase0) TPL_TRACE(k, 1);
                         const uint32_t sw = smem_addr(smem + stage * C::STAGE);
                         const uint32_t sx = sw + C::W_BYTES;
 #pragma unroll
@@ -689,7 +709,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 epi_sync();                     // this CTA's partial of the tile is written
                 const bool skip = cta == p.skip_cta && k == p.skip_phase && uc == first_uc + 1;
                 if (leader && !dead && !skip) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
+                if (leader && uc == first_uc + 1) TPL_TRACE(k, 2);
             }
+            if (leader) TPL_TRACE(k, 3);
             if (p.parallel && ph.kind == K_OPROJ) continue;    // finalized with down
             // pass 2: the phase's (tile, token) pairs, m_tiles x B in
             // tile-major order, are split evenly over the CTAs; CTA c
@@ -758,6 +780,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (helper && !dead && !prev_done &&
                     !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns))
                     fail();
+                if (leader && !prev_done) TPL_TRACE(k, 4);
                 prev_done = true;
                 epi_sync();                     // every segment of the tile is visible
                 if (dead || *labort) { epi_sync(); continue; }
@@ -897,6 +920,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 epi_sync();
                 if (leader && !dead)
                     publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)(t_hi - t_lo));
+                if (leader) TPL_TRACE(k, 5);
             }
         }
     }
@@ -982,6 +1006,16 @@ cudaError_t launch_np(const FusedMaps& maps, const FusedParams& prm, cudaStream_
 }
 
 }  // namespace
+
+bool fused_trace_read(void* host, size_t bytes) {
+#ifdef TPL_FUSED_TRACE
+    return bytes <= sizeof(g_fused_trace) && cudaMemcpyFromSymbol(host, g_fused_trace, bytes) == cudaSuccess;
+#else
+    (void)host;
+    (void)bytes;
+    return false;
+#endif
+}
 
 void fused_test_fault(int cta, int phase, long long wait_ns) {
     g_skip_cta = cta;

@@ -98,3 +98,14 @@ def test_short_wait_limit_alone_changes_nothing():
     torch.cuda.synchronize()
     assert tpl.device_status() == 0
     assert torch.equal(y, ref)
+
+
+def test_phase_trace_is_only_in_the_instrumented_build():
+    """The normal library records no phase stamps: the read is refused."""
+    import ctypes
+    buf = (ctypes.c_uint64 * 8)()
+    st = tpl.lib.tpl_fused_trace_read(ctypes.cast(buf, ctypes.c_void_p), ctypes.sizeof(buf))
+    if tpl.LIB_PATH.endswith("libtpl_trace.so"):
+        assert st == 0
+    else:
+        assert tpl.STATUS[st] == "TPL_ERR_UNSUPPORTED"
