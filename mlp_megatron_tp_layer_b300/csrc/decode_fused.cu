@@ -119,7 +119,7 @@ struct FCfg {
     static constexpr int STAGE = W_BYTES + X_BYTES;
     static constexpr int CTRL = 1024;                            // mbarriers and flags
     static constexpr int EPI = (2 * kFusedGridCap + 8) * 4;     // two segment lists and their counts
-    static constexpr int FIN_ITEMS = NP == 32 ? 10 : 12;         // float4 rows (of 32 lanes) a finalizing warp stages
+    static constexpr int FIN_ITEMS = NP == 32 ? 10 : 12;   // float4 rows (of 32 lanes) a finalizing warp stages
     static constexpr int FIN = 4 * FIN_ITEMS * 32 * 16;          // finalize staging, all epilogue warps
     static constexpr int STAGES_RAW = (kSmemLimit - 1024 - CTRL - EPI - FIN) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
@@ -340,6 +340,19 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// This lane's share of token t's RMSNorm tile sums (tiles lane, lane+32, ...,
+// added in that order).  The first two loads are issued together, so the
+// usual D <= 8192 costs one round trip, not one per tile.
+__device__ __forceinline__ float tile_sums(const float* sl, int Dt, int B, int t, int lane) {
+    const float a0 = lane < Dt ? __ldcg(sl + lane * B + t) : 0.f;
+    const float a1 = lane + 32 < Dt ? __ldcg(sl + (lane + 32) * B + t) : 0.f;
+    float s = 0.f;
+    s += a0;
+    s += a1;
+    for (int m2 = lane + 64; m2 < Dt; m2 += 32) s += __ldcg(sl + m2 * B + t);
+    return s;
 }
 
 // Packed-QKV rows r0 .. r0+3 (one head: hd % 64 == 0) of token t, rounded
@@ -861,9 +874,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                             if (t < t_hi) {
                                 if (has_resid && r0 < D)
                                     rv[j] = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
-                                if constexpr (NO) {
-                                    for (int m2 = lane; m2 < Dt; m2 += 32) ssq[j] += __ldcg(sl + m2 * B + t);
-                                }
+                                if constexpr (NO) ssq[j] = tile_sums(sl, Dt, B, t, lane);
                             }
                         }
                         for (int s0 = 0; s0 < nseg; s0 += SB) {
