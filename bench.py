@@ -806,7 +806,7 @@ def run_prefill(args, tpl, dev, world, peaks, peak_kind, stream):
 
 
 TRACE_EVENTS = ("act_ready", "mma_start", "first_ticket", "drained", "fin_start", "published", "w_first",
-                "act_wait")
+                "act_wait", "mma_first_unit_done", "w_last", "acc_first", "act_last")
 
 
 def run_phase_trace(args):

@@ -380,14 +380,18 @@ tpl_status tpl_profile_read(int i, char* tag, size_t tag_len, float* ms);
  * Phase trace of the fused decode stack, for measurement only.  An
  * instrumented build of the library (build.py --trace: libtpl_trace.so, the
  * kernels compiled with TPL_FUSED_TRACE) records, for every CTA and phase of
- * its last fused launch, %globaltimer stamps (ns) of 8 events:
+ * its last fused launch, %globaltimer stamps (ns) of 12 events:
  *   0 the activation producer found the first unit's inputs final,
  *   1 the first MMA of the phase was issued, 2 the first unit was counted on
  *   its tile ticket, 3 the CTA drained its last unit of the phase, 4 its
  *   first finalize of the phase passed its waits, 5 it published its last
  *   finalized tile, 6 the weight producer issued its first tile of the
- *   phase, 7 the activation producer began waiting for the phase's inputs.
- * Layout [148 CTAs][1 + 4*32 phases][8 events] uint64, 0 = not reached.
+ *   phase, 7 the activation producer began waiting for the phase's inputs,
+ *   8 the MMA issuer committed the phase's first unit, 9 the weight
+ *   producer issued its last tile of the phase, 10 the epilogue saw the
+ *   first unit's accumulator full, 11 the activation producer issued its
+ *   last activation tile of the phase.
+ * Layout [148 CTAs][1 + 4*32 phases][12 events] uint64, 0 = not reached.
  * tpl_fused_trace_read synchronises the device and copies up to `bytes` of
  * it to host memory; the normal build returns TPL_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------ */

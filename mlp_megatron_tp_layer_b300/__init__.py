@@ -425,7 +425,7 @@ def test_fused_fault(cta: int = -1, phase: int = 1, wait_limit_ns: int = 0):
     _check(lib.tpl_test_fused_fault(cta, phase, wait_limit_ns), "tpl_test_fused_fault")
 
 
-FUSED_TRACE_SHAPE = (148, 129, 8)    # CTAs, phases, events (see tpl_fused_trace_read)
+FUSED_TRACE_SHAPE = (148, 129, 12)    # CTAs, phases, events (see tpl_fused_trace_read)
 
 
 def fused_trace():

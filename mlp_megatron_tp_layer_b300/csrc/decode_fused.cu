@@ -506,6 +506,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const uint32_t fb = smem_addr(&full_w[stage]);
                 mbar_expect_tx(fb, C::W_BYTES);
                 tma_load_hint(smem_addr(smem + stage * C::STAGE), map, fb, x, y, pol);
+                TPL_TRACE(ld.k, 9);
                 last_par[stage] = (int)par;
                 if (++stage == C::STAGES) { stage = 0; par ^= 1; }
             }
@@ -558,6 +559,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                 int ax, ay;
                                 act_coord(p, ph, kb, ax, ay);
                                 tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, ax, ay, pol);
+                                TPL_TRACE(k, 11);
                             } else {
                                 mbar_arrive(fb);
                             }
@@ -633,6 +635,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                     if (!ok) break;
                     mma_commit(smem_addr(&acc_full[a]));
+                    if (uc == uc_phase0) TPL_TRACE(k, 8);
                     ++uc;
                 }
             }
@@ -700,6 +703,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const bool got = dead ? false : mbar_wait(smem_addr(&acc_full[a]), (uc >> 1) & 1, labort, gabort, p.wait_ns);
                 dead = !__all_sync(0xFFFFFFFFu, got);
                 if (dead && lane == 0) fail();
+                if (leader && uc == first_uc) TPL_TRACE(k, 10);
                 float* slot = p.part + ((size_t)ph.kind * region + cta + mt) * C::PART_FLOATS;
                 if (!dead) {
                     tc_fence_after();

@@ -195,7 +195,7 @@ struct FusedShape {
 bool fused_stack_shape_ok(const FusedShape& s);
 size_t fused_stack_ws_bytes(const FusedShape& s);
 // Phase trace of instrumented builds (tpl_fused_trace_read); false otherwise.
-constexpr int kFusedTraceEvents = 8;
+constexpr int kFusedTraceEvents = 12;
 bool fused_trace_read(void* host, size_t bytes);
 // Test hook behind tpl_test_fused_fault (cta < 0: off; wait_ns <= 0: default limit).
 void fused_test_fault(int cta, int phase, long long wait_ns);
