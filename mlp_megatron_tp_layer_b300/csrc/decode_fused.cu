@@ -53,6 +53,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <type_traits>
 
@@ -110,6 +111,7 @@ struct FusedParams {
     unsigned* err;
     uint64_t wait_ns;          // time limit of every wait between CTAs and roles
     int skip_cta, skip_phase;  // test hook: that CTA does not count its first unit of that phase (-1: off)
+    int s_cap[4];              // most segments a tile of each projection kind is split into
 };
 
 template <int NP>
@@ -197,7 +199,8 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     // traffic per tile; the CTAs left over stream no weights in this phase)
     ph.gw = p.G;
     const int s = min(p.G / ph.m_tiles, ph.nkb);
-    if (s >= 1 && ph.m_tiles * s * 100 >= p.G * 94) ph.gw = ph.m_tiles * s;
+    if (s > p.s_cap[ph.kind]) ph.gw = ph.m_tiles * p.s_cap[ph.kind];
+    else if (s >= 1 && ph.m_tiles * s * 100 >= p.G * 94) ph.gw = ph.m_tiles * s;
     return ph;
 }
 
@@ -951,6 +954,32 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
 
 int np_for(int64_t B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : 128; }
 
+// Most segments per tile, per projection kind.  A tile split over s CTAs
+// streams its weights s times faster but leaves s fp32 partials per token to
+// add up, and the finalize is spread over the whole grid.  With one CTA's
+// weight stream at about 44 GB/s and its finalize at R GB/s, a phase of W
+// weight bytes and m tiles takes about
+//     W / (m s 44) + m B s 512 PL / (G R)
+// and the best s is the square root of the ratio of the two coefficients.
+// The finalize is latency-bound (each batch of staged loads is one round
+// trip, and a batch carries more tokens as B grows): R = 10 sqrt(B / 32)
+// fits the Qwen2.5-1.5B-shaped stack at 32 and 64 tokens.  Phases with many
+// weight bytes per tile (every phase below ~16 tokens, every Llama-3.1-70B-
+// shaped phase) get a cap above the grid's own split, which then stands.
+void segment_caps(const FusedShape& sh, int G, int (&cap)[4]) {
+    const double B = (double)sh.B, D = (double)sh.D, F = (double)sh.F;
+    const double n_qkv = (double)(sh.n_q + 2 * sh.n_kv) * sh.hd, ko = (double)sh.n_q * sh.hd;
+    const double W[4] = {n_qkv * D * 2, D * ko * 2, 2 * F * D * 2, D * F * 2};
+    const double M[4] = {n_qkv, D, F, D};
+    const double PL[4] = {1, 1, 2, 1};
+    for (int k = 0; k < 4; ++k) {
+        const double m = std::ceil(M[k] / 128);
+        const double R = 10.0 * std::sqrt(B / 32.0);
+        const double best = std::sqrt(W[k] * G * R / (m * m * B * 512 * PL[k] * 44.0));
+        cap[k] = (int)std::max(1.0, std::min(1e6, std::floor(best + 0.5)));
+    }
+}
+
 // Test hook state (set by tpl_test_fused_fault): the next launches' wait
 // limit and the CTA / phase whose first ticket arrival is left out.
 std::atomic<int> g_skip_cta{-1}, g_skip_phase{-1};
@@ -1103,6 +1132,7 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
     prm.wait_ns = g_wait_ns > 0 ? (uint64_t)g_wait_ns : kWaitLimitNs;
     prm.skip_cta = g_skip_cta;
     prm.skip_phase = g_skip_phase;
+    segment_caps(s, G, prm.s_cap);
     prm.y_out = static_cast<__nv_bfloat16*>(y);
 
     FusedMaps maps;

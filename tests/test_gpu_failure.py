@@ -37,15 +37,13 @@ SHAPE = dict(D=1024, F=2048, n_q=8, n_kv=2, hd=128, tp=2, L=2)
 GRID = 148
 
 
-def last_cta_with_work(M, K, G=GRID):
-    """The fused stack gives a projection of M output rows and depth K to
-    g = m_tiles x s CTAs (every 128-row tile split into s k-ranges) when that
-    still covers 94% of the G CTAs, else to all G; the last of them always
-    holds the phase's last (m-tile, k-block) pair."""
-    m_tiles, nkb = -(-M // 128), -(-K // 64)
-    s = min(G // m_tiles, nkb)
-    g = m_tiles * s if s >= 1 and m_tiles * s * 100 >= G * 94 else G
-    return g - 1
+def cta_with_work(M, G=GRID):
+    """A CTA that holds units of a projection of M output rows whatever split
+    the fused stack picks: a phase goes to m_tiles x s CTAs (every 128-row
+    tile in s k-ranges, s >= 1), or is spread over the whole grid when it has
+    at least G (m-tile, k-block) pairs (true of every phase used here), so
+    CTAs 0 .. min(m_tiles, G) - 1 always have work; this is the last of them."""
+    return min(-(-M // 128), G) - 1
 
 
 _S = SHAPE
@@ -66,10 +64,10 @@ def _stack(B, block):
 
 # (cta, phase): phase 4 l + 1 + j is projection j of layer l in the block's order
 @pytest.mark.parametrize("B,block,cta,phase", [
-    (1, tpl.BLOCK_SERIAL, last_cta_with_work(_QKV_ROWS, _S["D"]), 1),                  # QKV of layer 0
+    (1, tpl.BLOCK_SERIAL, cta_with_work(_QKV_ROWS), 1),                  # QKV of layer 0
     (40, tpl.BLOCK_SERIAL, 0, 3),                                                       # gate/up of layer 0
-    (1, tpl.BLOCK_SERIAL, last_cta_with_work(_S["D"], _S["F"]), 8),                     # down of layer 1
-    (16, tpl.BLOCK_PARALLEL, last_cta_with_work(_S["D"], _S["n_q"] * _S["hd"]), 3),     # o_proj, finalized with down
+    (1, tpl.BLOCK_SERIAL, cta_with_work(_S["D"]), 8),                     # down of layer 1
+    (16, tpl.BLOCK_PARALLEL, cta_with_work(_S["D"]), 3),     # o_proj, finalized with down
 ])
 def test_fused_stack_wait_runs_out_and_the_next_call_is_clean(B, block, cta, phase):
     run = _stack(B, block)
