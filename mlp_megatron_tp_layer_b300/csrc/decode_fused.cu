@@ -137,6 +137,7 @@ struct FCfg {
 struct Phase {
     int kind, layer, m_tiles, nkb, M;
     int gw;                    // CTAs holding units of the phase: 0 .. gw-1
+    int whole;                 // tiles 0 .. whole-1 go whole to CTAs 0 .. whole-1 (0: none)
     int prev_fin;              // phase whose completion this phase's finalize waits for (-1: none)
     int src_kind;              // kind whose output tiles the activation loads wait for (-1: launch input)
     unsigned src_target;       // ready count of such a tile once this layer's input is final
@@ -150,6 +151,7 @@ struct Phase {
 // block: QKV, o_proj, gate/up, down.  Parallel block: QKV and gate/up (both
 // on RMSNorm(x)), then o_proj and down, whose partials are summed together
 // into y by down's finalize (o_proj finalizes nothing of its own).
+template <bool WH = false>
 __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams& p, int k) {
     Phase ph;
     ph.layer = (k - 1) >> 2;
@@ -198,6 +200,13 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     // cover at least 94% of the grid (fewer, aligned segments: less partial
     // traffic per tile; the CTAs left over stream no weights in this phase)
     ph.gw = p.G;
+    // gate/up with at least one tile per CTA: CTA c first takes tile c whole
+    // (its SwiGLU comes straight from TMEM, no partials), then its share of
+    // the remaining tiles, split as below
+    // (only the 128-column instantiation carries this path: it pays at 65-128
+    // tokens, where the gate/up finalize is long)
+    ph.whole = (WH && ph.kind == K_GATEUP && ph.m_tiles >= p.G) ? p.G : 0;
+    if (ph.whole) return ph;
     const int s = min(p.G / ph.m_tiles, ph.nkb);
     if (s > p.s_cap[ph.kind]) ph.gw = ph.m_tiles * p.s_cap[ph.kind];
     else if (s >= 1 && ph.m_tiles * s * 100 >= p.G * 94) ph.gw = ph.m_tiles * s;
@@ -259,16 +268,39 @@ __device__ __forceinline__ bool has_work(int64_t total, int G, int c) {
     return total * (c + 1) / G > total * c / G;
 }
 
-// The units (m-tile, k-block range) of CTA c in a phase, in k order.
+// The split part of a phase: the flattened (m-tile, k-block) pairs from
+// index seg_base on (the tiles after the whole ones), seg_total of them,
+// split over CTAs 0 .. gw-1.
+__device__ __forceinline__ int64_t seg_base(const Phase& ph) { return (int64_t)ph.whole * ph.nkb; }
+__device__ __forceinline__ int64_t seg_total(const Phase& ph) { return ph.total - seg_base(ph); }
+
+// The units (m-tile, k-block range) of CTA c in a phase, in k order: its
+// whole tile if it has one (WH), then its range [idx2, hi2) of the split part.
+template <bool WH>
 struct Units {
-    int64_t idx, hi;
+    int64_t idx, hi, idx2, hi2;
     int nkb;
-    __device__ __forceinline__ Units() : idx(0), hi(0), nkb(1) {}
-    __device__ __forceinline__ Units(const Phase& ph, int c)
-        : idx(c < ph.gw ? ph.total * c / ph.gw : 0), hi(c < ph.gw ? ph.total * (c + 1) / ph.gw : 0),
-          nkb(ph.nkb) {}
+    __device__ __forceinline__ Units() : idx(0), hi(0), idx2(0), hi2(0), nkb(1) {}
+    __device__ __forceinline__ Units(const Phase& ph, int c) : nkb(ph.nkb) {
+        if constexpr (WH) {
+            const int64_t b = seg_base(ph), t = seg_total(ph);
+            idx = c < ph.whole ? (int64_t)c * ph.nkb : 0;
+            hi = c < ph.whole ? idx + ph.nkb : 0;
+            idx2 = c < ph.gw ? b + t * c / ph.gw : 0;
+            hi2 = c < ph.gw ? b + t * (c + 1) / ph.gw : 0;
+        } else {
+            idx = c < ph.gw ? ph.total * c / ph.gw : 0;
+            hi = c < ph.gw ? ph.total * (c + 1) / ph.gw : 0;
+            idx2 = hi2 = 0;
+        }
+    }
     __device__ __forceinline__ bool next(int& mt, int& kb0, int& kb1) {
-        if (idx >= hi) return false;
+        if (idx >= hi) {
+            if (!WH || idx2 >= hi2) return false;
+            idx = idx2;
+            hi = hi2;
+            idx2 = hi2 = 0;
+        }
         mt = (int)(idx / nkb);
         kb0 = (int)(idx - (int64_t)mt * nkb);
         kb1 = (int)min((int64_t)nkb, (int64_t)kb0 + (hi - idx));
@@ -279,10 +311,11 @@ struct Units {
 
 // Walks the weight tiles this CTA loads, in load order, across phases and
 // layers (a gate/up k-block is two tiles: gate, then up).
+template <bool WH>
 struct TileCursor {
     int k;
     Phase ph;
-    Units u;
+    Units<WH> u;
     int mt, kb, kb1, hf;
     __device__ __forceinline__ bool next(const FusedMaps& mp, const FusedParams& p, int G, int cta, int n_phases,
                                          const CUtensorMap*& map, int& x, int& y) {
@@ -297,8 +330,8 @@ struct TileCursor {
             int kb0;
             if (k >= 1 && u.next(mt, kb0, kb1)) { kb = kb0; hf = 0; continue; }
             if (++k >= n_phases) return false;
-            ph = phase_of(mp, p, k);
-            u = Units(ph, cta);
+            ph = phase_of<WH>(mp, p, k);
+            u = Units<WH>(ph, cta);
             kb = kb1 = 0;
         }
     }
@@ -440,6 +473,7 @@ template <int NP>
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     using C = FCfg<NP>;
+    constexpr bool WH = NP == 128;       // gate/up tiles taken whole when there are at least G of them
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ctrl = smem + C::STAGES * C::STAGE;
@@ -494,7 +528,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         // layer boundaries (weights never depend on activations).
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            TileCursor ld{};
+            TileCursor<WH> ld{};
             int stage = 0;
             uint32_t par = 0;
             int last_par[C::STAGES];           // parity of the latest copy issued into each stage, -1: none
@@ -539,40 +573,43 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         for (int s = 0; s < C::STAGES; ++s) last_par[s] = -1;
         bool ok = true;
         for (int k = 1; k < n_phases && ok; ++k) {
-            const Phase ph = phase_of(mp, p, k);
+            const Phase ph = phase_of<WH>(mp, p, k);
             const int halves = ph.kind == K_GATEUP ? 2 : 1;
-            const Units u(ph, cta);            // this CTA's pairs [u.idx, u.hi), in k order per m-tile
-            for (int64_t idx = u.idx; ok && idx < u.hi;) {
-                int n = (int)min(u.hi - idx, (int64_t)32);
-                const bool first_k = idx == u.idx;
-                if (first_k && lane == 0) TPL_TRACE(k, 7);
-                if (ph.src_kind >= 0) {
-                    n = ready_prefix(p, ph, idx, u.hi, lane, labort, gabort);
-                    if (n == 0) { ok = false; break; }
-                }
-                if (first_k && lane == 0) TPL_TRACE(k, 0);
-                if (lane == 0) {
-                    for (int j = 0; j < n && ok; ++j) {
-                        const int kb = (int)((idx + j) % ph.nkb);
-                        for (int hf = 0; hf < halves; ++hf) {
-                            if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
-                            const uint32_t fb = smem_addr(&full_x[stage]);
-                            if (hf == 0) {
-                                mbar_expect_tx(fb, C::X_BYTES);
-                                int ax, ay;
-                                act_coord(p, ph, kb, ax, ay);
-                                tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, ax, ay, pol);
-                                TPL_TRACE(k, 11);
-                            } else {
-                                mbar_arrive(fb);
+            const Units<WH> u(ph, cta);        // this CTA's pairs: [u.idx, u.hi) then [u.idx2, u.hi2)
+            for (int range = 0; range < (WH ? 2 : 1) && ok; ++range) {
+                const int64_t r_lo = range ? u.idx2 : u.idx, r_hi = range ? u.hi2 : u.hi;
+                for (int64_t idx = r_lo; ok && idx < r_hi;) {
+                    int n = (int)min(r_hi - idx, (int64_t)32);
+                    const bool first_k = idx == (u.idx < u.hi ? u.idx : u.idx2);
+                    if (first_k && lane == 0) TPL_TRACE(k, 7);
+                    if (ph.src_kind >= 0) {
+                        n = ready_prefix(p, ph, idx, r_hi, lane, labort, gabort);
+                        if (n == 0) { ok = false; break; }
+                    }
+                    if (first_k && lane == 0) TPL_TRACE(k, 0);
+                    if (lane == 0) {
+                        for (int j = 0; j < n && ok; ++j) {
+                            const int kb = (int)((idx + j) % ph.nkb);
+                            for (int hf = 0; hf < halves; ++hf) {
+                                if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
+                                const uint32_t fb = smem_addr(&full_x[stage]);
+                                if (hf == 0) {
+                                    mbar_expect_tx(fb, C::X_BYTES);
+                                    int ax, ay;
+                                    act_coord(p, ph, kb, ax, ay);
+                                    tma_load_hint(smem_addr(smem + stage * C::STAGE + C::W_BYTES), ph.act, fb, ax, ay, pol);
+                                    TPL_TRACE(k, 11);
+                                } else {
+                                    mbar_arrive(fb);
+                                }
+                                last_par[stage] = (int)par;
+                                if (++stage == C::STAGES) { stage = 0; par ^= 1; }
                             }
-                            last_par[stage] = (int)par;
-                            if (++stage == C::STAGES) { stage = 0; par ^= 1; }
                         }
                     }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                    idx += n;
                 }
-                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-                idx += n;
             }
         }
         if (!ok && lane == 0) {
@@ -593,9 +630,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             int uc = 0;
             bool ok = true;
             for (int k = 1; k < n_phases && ok; ++k) {
-                const Phase ph = phase_of(mp, p, k);
+                const Phase ph = phase_of<WH>(mp, p, k);
                 const bool dual = ph.kind == K_GATEUP;
-                Units u(ph, cta);
+                Units<WH> u(ph, cta);
                 int mt, kb0, kb1;
                 const int uc_phase0 = uc;
                 while (ok && u.next(mt, kb0, kb1)) {
@@ -685,7 +722,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         const size_t region = (size_t)(kFusedGridCap + p.max_mt);    // partial slots per projection kind
         int uc = 0;
         for (int k = 1; k < n_phases; ++k) {
-            const Phase ph = phase_of(mp, p, k);
+            const Phase ph = phase_of<WH>(mp, p, k);
             const bool dual = ph.kind == K_GATEUP;
             const int planes = dual ? 2 : 1;
             const int l = ph.layer;
@@ -694,12 +731,15 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // down tile's ticket and its finalize
             const bool merged = p.parallel && ph.kind == K_DOWN;
             const int tk_kind = (p.parallel && ph.kind == K_OPROJ) ? K_DOWN : ph.kind;
-            Units u(ph, cta);
+            Units<WH> u(ph, cta);
             int mt, kb0, kb1;
             const int first_uc = uc;
+            // the serial block's MLP normalises h, everything else the layer input
+            const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
             // pass 1: drain every unit into its partial slot and count it on
             // its tile's ticket (no waiting here, so tiles never wait on one
-            // another through a CTA that holds pieces of two of them)
+            // another through a CTA that holds pieces of two of them); a whole
+            // gate/up tile is finished here instead
             while (u.next(mt, kb0, kb1)) {
                 const int a = uc & 1;
                 dead = dead || *labort || *gabort;
@@ -708,7 +748,46 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (dead && lane == 0) fail();
                 if (leader && uc == first_uc) TPL_TRACE(k, 10);
                 float* slot = p.part + ((size_t)ph.kind * region + cta + mt) * C::PART_FLOATS;
-                if (!dead) {
+                const bool whole = WH && mt < ph.whole;  // the same in every epilogue warp
+                if (whole) {
+                    // h = SwiGLU of the RMSNorm-scaled accumulators, as a finalize
+                    // computes it.  Every tile sum of the norm's input is final
+                    // once the phase before this one has finished.
+                    if (helper && !dead && ph.prev_fin >= 0 &&
+                        !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns))
+                        fail();
+                    epi_sync();
+                    dead = dead || *labort;
+                    float* scl = reinterpret_cast<float*>(seg);     // per-token scales (the segment lists are idle)
+                    if (!dead) {
+                        for (int t = q; t < B; t += 4) {
+                            const float ss = warp_sum32(tile_sums(sl, Dt, B, t, lane));
+                            if (lane == 0) scl[t] = 1.0f / sqrtf(ss / (float)D + p.eps);
+                        }
+                    }
+                    epi_sync();
+                    if (!dead) {
+                        tc_fence_after();
+                        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
+                        const int r0 = mt * 128 + row;
+#pragma unroll 1
+                        for (int c0 = 0; c0 < NP && c0 < B; c0 += 16) {
+                            float g[32], up[32];            // (16 columns used)
+                            tmem_ld16(tb + c0, g);
+                            tmem_ld16(tb + NP + c0, up);
+                            if (r0 < p.F) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int t = c0 + j;
+                                    if (t < B) {
+                                        const float sc = scl[t];
+                                        p.H[(int64_t)t * p.F + r0] = __float2bfloat16_rn(silu_f(g[j] * sc) * (up[j] * sc));
+                                    }
+                                }
+                            }
+                        }
+                    }
+                } else if (!dead) {
                     tc_fence_after();
                     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
                     for (int pl = 0; pl < planes; ++pl) {
@@ -726,9 +805,13 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&acc_empty[a]));
                 ++uc;
-                epi_sync();                     // this CTA's partial of the tile is written
+                epi_sync();                     // this CTA's partial of the tile (or the whole tile) is written
                 const bool skip = cta == p.skip_cta && k == p.skip_phase && uc == first_uc + 1;
-                if (leader && !dead && !skip) red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
+                if (whole) {
+                    if (leader && !dead && !skip) publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)B);
+                } else if (leader && !dead && !skip) {
+                    red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
+                }
                 if (leader && uc == first_uc + 1) TPL_TRACE(k, 2);
             }
             if (leader) TPL_TRACE(k, 3);
@@ -745,14 +828,15 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // which hold work unless the phase has fewer pairs than CTAs (then
             // warp 2 lists the ones that do into list / seg_info[info])
             auto seg_list = [&](const Phase& phx, int mt_, int* list, int info, int& cf_, bool& every_) {
-                every_ = phx.total >= phx.gw;
-                cf_ = owner_of((int64_t)mt_ * phx.nkb, phx.total, phx.gw);
-                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1, phx.total, phx.gw);
+                const int64_t sb = seg_base(phx), st = seg_total(phx);
+                every_ = st >= phx.gw;
+                cf_ = owner_of((int64_t)mt_ * phx.nkb - sb, st, phx.gw);
+                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1 - sb, st, phx.gw);
                 if (!every_ && warp == 2) {
                     int n = 0;
                     for (int base = cf_; base <= cl_; base += 32) {
                         const int cc = base + lane;
-                        const bool w = cc <= cl_ && has_work(phx.total, phx.gw, cc);
+                        const bool w = cc <= cl_ && has_work(st, phx.gw, cc);
                         const unsigned m = __ballot_sync(0xFFFFFFFFu, w);
                         if (w) list[n + __popc(m & ((1u << lane) - 1u))] = cc + mt_;
                         n += __popc(m);
@@ -761,19 +845,19 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 }
                 return cl_;
             };
-            const Phase ph_o = merged ? phase_of(mp, p, k - 1) : ph;       // the o_proj phase of the layer
+            const Phase ph_o = merged ? phase_of<WH>(mp, p, k - 1) : ph;   // the o_proj phase of the layer
             const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
-            // the serial block's MLP normalises h, everything else the layer input
-            const float* sl = (ph.kind == K_GATEUP && !p.parallel) ? p.slots_h : p.slots_y;
             bool prev_done = ph.prev_fin < 0;
-            const int64_t npairs = (int64_t)ph.m_tiles * B;
+            // (tiles before ph.whole were finished whole in pass 1)
+            const int64_t npairs = (int64_t)(ph.m_tiles - ph.whole) * B;
             const int64_t f1 = npairs * (cta + 1) / G;
             for (int64_t f = npairs * cta / G; f < f1;) {
-                mt = (int)(f / B);
+                const int64_t fm = f / B;               // tile index among the split tiles
+                mt = ph.whole + (int)fm;
                 // this CTA's tokens of tile mt
-                const int t_lo = (int)(f - (int64_t)mt * B);
-                const int t_hi = (int)min((int64_t)B, f1 - (int64_t)mt * B);
-                f = (int64_t)mt * B + t_hi;
+                const int t_lo = (int)(f - fm * B);
+                const int t_hi = (int)min((int64_t)B, f1 - fm * B);
+                f = fm * B + t_hi;
                 int cf, cf_o = 0;
                 bool every, every_o = true;
                 const int cl = seg_list(ph, mt, seg, 0, cf, every);

@@ -286,6 +286,24 @@ def test_decoder_stack_fused_in_place_and_gqa_shapes(B):
     assert_within(y, ref, stack_allowance(trace, ref), what="in-place fused stack")
 
 
+# gate/up with at least one 128-row tile per CTA (149 tiles): CTA c takes tile c
+# whole and applies SwiGLU from TMEM; the remaining tile is split over the grid
+@pytest.mark.parametrize("B", [1, 40, 128])
+@pytest.mark.parametrize("block", ["serial", "parallel"])
+def test_decoder_stack_fused_whole_gateup_tiles(B, block):
+    D, F, n_q, n_kv, hd, tp, L = 256, 19072, 2, 1, 128, 2, 2
+    x = si.activations(B, D, seed=12, device="cuda")
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=12, layer=l, sigma=0.03, device="cuda") for l in range(L)]
+    trace = []
+    ref = O.decoder_stack(to_np(x), [{k: to_np(v) for k, v in W.items()} for W in layers], n_q, n_kv, hd, tp,
+                          trace=trace, block=block)
+    blk = tpl.BLOCK_PARALLEL if block == "parallel" else tpl.BLOCK_SERIAL
+    y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, path=tpl.PATH_FUSED, block=blk)
+    assert_within(y, ref, stack_allowance(trace, ref), what="fused stack, whole gate/up tiles")
+    y2 = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, path=tpl.PATH_FUSED, block=blk)
+    assert_equal(y2, to_np(y), what="second run")
+
+
 # ------------------------------------------ parallel (PaLM) block, [L4] S5.5
 
 @pytest.mark.parametrize("B", [1, 5, 17, 32, 40, 64, 128])
