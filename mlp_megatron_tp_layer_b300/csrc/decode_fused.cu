@@ -935,8 +935,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                 };
                 auto add4 = [](float4& a, const float4& b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; };
-                // A warp takes TB of its tokens at a time (TB = 2 when their
-                // segments fit its staging rows, else 1).  Each lane copies
+                // A warp takes TB of its tokens at a time (TB = 2, or 3 in the
+                // 128-column instantiation, when their segments fit its staging
+                // rows, else 1).  Each lane copies
                 // its own 16 bytes (4 rows) of every partial segment of the
                 // batch's tokens (both planes for gate/up) into the warp's
                 // staging rows with cp.async, up to SB segments per token and
@@ -1008,6 +1009,11 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 using I2 = std::integral_constant<int, 2>;
                 auto share = [&](auto dual_c, auto norm_c) {
                     constexpr int PL = decltype(dual_c)::value ? 2 : 1;
+                    // three tokens a batch at 128 columns, where a CTA finalizes ~60-200 pairs
+                    if (NP == 128 && 3 * PL * nseg <= C::FIN_ITEMS) {
+                        share_tb(std::integral_constant<int, 3>{}, dual_c, norm_c);
+                        return;
+                    }
                     if (NP > 32 && 2 * PL * nseg <= C::FIN_ITEMS) share_tb(I2{}, dual_c, norm_c);
                     else share_tb(I1{}, dual_c, norm_c);
                 };
