@@ -382,8 +382,9 @@ tpl_status tpl_profile_read(int i, char* tag, size_t tag_len, float* ms);
  * kernels compiled with TPL_FUSED_TRACE) records, for every CTA and phase of
  * its last fused launch, %globaltimer stamps (ns) of 12 events:
  *   0 the activation producer found the first unit's inputs final,
- *   1 the first MMA of the phase was issued, 2 the first unit was counted on
- *   its tile ticket, 3 the CTA drained its last unit of the phase, 4 its
+ *   1 the first MMA of the phase was issued, 2 the first unit was delivered
+ *   (counted on its tile ticket, or its tagged words stored), 3 the CTA
+ *   drained its last unit of the phase, 4 its
  *   first finalize of the phase passed its waits, 5 it published its last
  *   finalized tile, 6 the weight producer issued its first tile of the
  *   phase, 7 the activation producer began waiting for the phase's inputs,
@@ -404,20 +405,23 @@ tpl_status tpl_fused_trace_read(void* host, size_t bytes);
  * hang and timeout modes of the TP serving pages) -- and this makes that
  * happen on one GPU without a fault.
  *
- * Every wait of the fused stack (between CTAs: tile tickets, tile readiness,
- * phase completion; inside a CTA: the mbarriers of its pipeline) gives up
+ * Every wait of the fused stack (between CTAs: tile tickets or tagged partial
+ * words, tile readiness, phase completion; inside a CTA: the mbarriers of its
+ * pipeline and the phase watcher's posts) gives up
  * after a time limit, raises the launch's abort flag so that every CTA stops
  * waiting, drains its copies and MMAs in flight, frees its tensor memory and
  * returns; the sticky device error word then holds TPL_DEVERR_TIMEOUT
  * (tpl_device_status).  tpl_test_fused_fault(cta, phase, wait_limit_ns)
  * applies to the fused-stack launches issued after it:
- *   - cta >= 0: CTA `cta` does not count its first unit of phase `phase`
+ *   - cta >= 0: CTA `cta` does not deliver its first unit of phase `phase`
  *     (>= 1; phase 4 l + 1 + j is projection j of layer l of the launch, in
- *     the block's phase order) on its tile's ticket, so the tile's finalize
- *     waits until the limit passes.  cta < 0 turns the omission off.
+ *     the block's phase order): no count on its tile's ticket or, up to 16
+ *     tokens, no tagged partial words, so the tile's finalize waits until
+ *     the limit passes.  cta < 0 turns the omission off.
  *   - wait_limit_ns > 0 sets the limit (10 us .. 2 s); <= 0 restores 2 s.
  * After such a launch the workspace needs nothing: the next launch starts
- * from zeroed counters and rewrites every buffer before reading it.
+ * from zeroed counters and tagged words and rewrites every buffer before
+ * reading it.
  * Returns TPL_ERR_UNSUPPORTED for arguments out of range.
  * ------------------------------------------------------------------------ */
 tpl_status tpl_test_fused_fault(int cta, int phase, int64_t wait_limit_ns);

@@ -17,12 +17,19 @@
 // with g = m_tiles x s (every tile exactly s segments) when that still uses
 // at least 94% of the G CTAs, else g = G.
 // A range may cover parts of several m-tiles ("units"); each unit leaves an
-// fp32 partial tile in global memory and counts itself on the tile's ticket.
-// Once all of a tile's units have arrived, the CTAs that hold them each
-// finalize a share of the tile's tokens: they add the tile's partials in k
-// order (the order of the shards for the row-parallel phases) and apply the
+// fp32 partial tile in global memory.  In the 32- to 128-column
+// instantiations it then counts itself on the tile's ticket (a release
+// increment), and a finalizing CTA waits for the count before it loads the
+// partials.  In the 16-column one (up to 16 tokens, where a phase is short
+// and that fence and ticket round trip are a large part of it) each partial
+// value is stored with a 32-bit tag (layer + 1) in one 8-byte word, which a
+// reader sees whole or not at all: the finalizer polls the words themselves
+// until every one carries this layer's tag, with no fence or counter in
+// between.  Once all of a tile's units have arrived, the CTAs that hold them
+// each finalize a share of the tile's tokens: they add the tile's partials in
+// k order (the order of the shards for the row-parallel phases) and apply the
 // phase's epilogue.  The sum is therefore the same whatever order the CTAs
-// ran in.
+// ran in, and the same in both exchanges.
 //
 // There is no grid-wide barrier between phases.  Each output tile of a phase
 // has a ready counter (tokens finalized, monotone over the layers of the
@@ -44,10 +51,12 @@
 // epilogue turns the tile sums into 1/rms and multiplies its fp32 products by
 // it (RMSNorm(x) W^T = diag(1/rms(x)) x W^T).
 //
-// Warp roles (224 threads): 0 weight TMA producer, 1 TMEM owner + MMA issuer,
+// Warp roles (256 threads): 0 weight TMA producer, 1 TMEM owner + MMA issuer,
 // 2..5 epilogue (warp w reads TMEM lanes 32 (w % 4) ..), 6 activation TMA
-// producer.  Every wait is bounded in time; on expiry the CTA sets the grid
-// abort flag and the sticky device error word, and every role winds down.
+// producer, 7 phase watcher (polls the done counters ahead of the epilogue
+// and posts, in shared memory, which phases may finalize).  Every wait is
+// bounded in time; on expiry the CTA sets the grid abort flag and the sticky
+// device error word, and every role winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -77,10 +86,13 @@ __device__ unsigned long long g_fused_trace[kFusedGridCap * kFusedTracePhases * 
 
 namespace {
 
-constexpr int kFThreads = 224;
+constexpr int kFThreads = 256;
 constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory of one CTA
-constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6;
+constexpr int kWarpW = 0, kWarpMma = 1, kWarpAct = 6, kWarpWatch = 7;
 constexpr int kTmemCols = 512;     // two accumulators of up to 256 columns
+// Instantiations up to this width exchange tagged partial words.  (At 32
+// columns, twice the words per unit and the longer polls lost 5-10%.)
+constexpr int kTaggedNP = 16;
 constexpr int kAccStride = 256;
 enum Kind { K_QKV = 0, K_OPROJ = 1, K_GATEUP = 2, K_DOWN = 3 };
 enum ActMap { A_X = 0, A_R0 = 1, A_R1 = 2, A_QKV = 3, A_H = 4, A_HID = 5, A_COUNT = 6 };
@@ -110,7 +122,7 @@ struct FusedParams {
     int* gabort;               // grid abort flag (zero at launch)
     unsigned* err;
     uint64_t wait_ns;          // time limit of every wait between CTAs and roles
-    int skip_cta, skip_phase;  // test hook: that CTA does not count its first unit of that phase (-1: off)
+    int skip_cta, skip_phase;  // test hook: that CTA does not deliver its first unit of that phase (-1: off)
     int s_cap[4];              // most segments a tile of each projection kind is split into
 };
 
@@ -369,6 +381,19 @@ __device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, vol
     }
 }
 
+// Tagged partial words (the 16-column instantiation): an fp32 partial and a
+// 32-bit tag (layer + 1) stored as one aligned 8-byte word, which a reader
+// sees whole or not at all, so a finalizer polls the data itself and the
+// writer needs neither a fence nor a ticket.
+__device__ __forceinline__ void st_tagged(uint64_t* a, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_tagged2(const uint64_t* a) {
+    ulonglong2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(a) : "memory");
+    return r;
+}
+
 // 16-byte global -> shared copy through L2 only (cp.async, no registers held
 // while it is in flight), and the wait for every copy this thread issued.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -474,6 +499,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     using C = FCfg<NP>;
     constexpr bool WH = NP == 128;       // gate/up tiles taken whole when there are at least G of them
+    constexpr bool LL = NP <= kTaggedNP;  // tagged partial words instead of tile tickets
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ctrl = smem + C::STAGES * C::STAGE;
@@ -485,6 +511,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 1000);
     volatile int* labort = reinterpret_cast<volatile int*>(ctrl + 1004);
+    int* fin_ok = reinterpret_cast<int*>(ctrl + 1008);         // latest phase whose previous finalizing phase is complete
     int* seg = reinterpret_cast<int*>(ctrl + C::CTRL);          // partial slots of the tile being finalized
     float4* fin_buf = reinterpret_cast<float4*>(ctrl + C::CTRL + C::EPI);   // [4 warps][FIN_ITEMS][32 lanes]
     int* seg2 = seg + kFusedGridCap;                            // ... of its o_proj part (parallel block)
@@ -507,6 +534,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         }
         mbar_init(smem_addr(drain), 1);
         *labort = 0;
+        *fin_ok = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -685,6 +713,23 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_addr(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {}
         }
+    } else if (warp == kWarpWatch) {
+        // ---------------------------------------------------- phase watcher
+        // Waits, phase after phase, until the phase that phase k's finalize
+        // follows is complete, and posts k in shared memory, so the finalizing
+        // warps find the answer there instead of polling global memory
+        // on their critical path.
+        if (lane == 0) {
+            for (int k = 1; k < n_phases; ++k) {
+                const Phase ph = phase_of<WH>(mp, p, k);
+                if (ph.prev_fin >= 0 &&
+                    !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns)) {
+                    fail();
+                    break;
+                }
+                asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(fin_ok)), "r"(k) : "memory");
+            }
+        }
     } else {
         // ---------------------------------------------------- epilogue (warps 2..5)
         // (warps 0, 1 and 6 have their own roles above)
@@ -695,6 +740,16 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         const int row = q * 32 + lane;                 // drain: row of the tile (TMEM lane)
         const bool leader = warp == 2 && lane == 0;
         const bool helper = warp == 3 && lane == 0;    // waits for the previous phase beside the leader
+        // bounded wait until the watcher has posted phase k (acquire)
+        auto posted = [&](int k) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t i = 0;; ++i) {
+                int v;
+                asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(fin_ok)) : "memory");
+                if (v >= k) return true;
+                if ((i & 15u) == 15u && (*labort || *gabort || globaltimer() - t0 > p.wait_ns)) return false;
+            }
+        };
         const int B = p.B, D = p.D;
         const int Dt = (D + 127) / 128;
         bool dead = false;
@@ -753,9 +808,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     // h = SwiGLU of the RMSNorm-scaled accumulators, as a finalize
                     // computes it.  Every tile sum of the norm's input is final
                     // once the phase before this one has finished.
-                    if (helper && !dead && ph.prev_fin >= 0 &&
-                        !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns))
-                        fail();
+                    if (helper && !dead && ph.prev_fin >= 0 && !posted(k)) fail();
                     epi_sync();
                     dead = dead || *labort;
                     float* scl = reinterpret_cast<float*>(seg);     // per-token scales (the segment lists are idle)
@@ -787,6 +840,25 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                             }
                         }
                     }
+                } else if (LL && !dead) {
+                    // [plane][token][row] tagged words; the test hook leaves one unit unwritten
+                    tc_fence_after();
+                    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
+                    const bool skip_w = cta == p.skip_cta && k == p.skip_phase && uc == first_uc;
+                    uint64_t* s64 = reinterpret_cast<uint64_t*>(p.part) +
+                                    ((size_t)ph.kind * region + cta + mt) * (size_t)(2 * B * 128);
+                    const uint64_t tag = (uint64_t)(l + 1) << 32;
+                    for (int pl = 0; pl < planes; ++pl) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < NP && c0 < B; c0 += C::CH) {
+                            float v[32];
+                            if (C::CH == 32) tmem_ld32(tb + pl * NP + c0, v); else tmem_ld16(tb + pl * NP + c0, v);
+#pragma unroll
+                            for (int j = 0; j < C::CH; ++j)
+                                if (c0 + j < B && !skip_w)
+                                    st_tagged(s64 + (size_t)(pl * B + c0 + j) * 128 + row, tag | __float_as_uint(v[j]));
+                        }
+                    }
                 } else if (!dead) {
                     tc_fence_after();
                     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + a * kAccStride;
@@ -809,7 +881,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 const bool skip = cta == p.skip_cta && k == p.skip_phase && uc == first_uc + 1;
                 if (whole) {
                     if (leader && !dead && !skip) publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)B);
-                } else if (leader && !dead && !skip) {
+                } else if (!LL && leader && !dead && !skip) {
                     red_release_add(p.tickets + tk_kind * p.max_mt + mt, 1u);
                 }
                 if (leader && uc == first_uc + 1) TPL_TRACE(k, 2);
@@ -878,12 +950,10 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 // every unit of the tile has arrived, and the phase finalized
                 // before this one is complete (so are all earlier ones: each
                 // waited likewise); two threads wait side by side
-                if (leader && !dead &&
+                if (!LL && leader && !dead &&
                     !grid_wait(p.tickets + tk_kind * p.max_mt + mt, (unsigned)nseg * (unsigned)(l + 1), labort, gabort, p.wait_ns))
                     fail();
-                if (helper && !dead && !prev_done &&
-                    !grid_wait(p.done + ph.prev_fin, done_target(mp, p, ph.prev_fin), labort, gabort, p.wait_ns))
-                    fail();
+                if (helper && !dead && !prev_done && !posted(k)) fail();
                 if (leader && !prev_done) TPL_TRACE(k, 4);
                 prev_done = true;
                 epi_sync();                     // every segment of the tile is visible
@@ -969,6 +1039,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                 if constexpr (NO) ssq[j] = tile_sums(sl, Dt, B, t, lane);
                             }
                         }
+                        {
                         for (int s0 = 0; s0 < nseg; s0 += SB) {
                             const int nb = min(SB, nseg - s0);
 #pragma unroll
@@ -997,6 +1068,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                                 }
                             }
                         }
+                        }
 #pragma unroll
                         for (int j = 0; j < TB; ++j) {
                             float sc = 1.f;
@@ -1005,28 +1077,148 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                         }
                     }
                 };
+                // 16 columns: the tile's tagged partial words are polled by all
+                // four warps at once (item i = token j x segment; warp i % 4 holds
+                // it in registers), checked, staged in shared memory, and added
+                // in k order by the token's warp (warp j of the round).  A round
+                // takes as many whole tokens as the staging holds (at most 4),
+                // or one token in chunks of segments.
+                auto share_ll = [&](auto dual_c, auto norm_c) {
+                    constexpr bool DU = decltype(dual_c)::value, NO = decltype(norm_c)::value;
+                    constexpr int PL = DU ? 2 : 1;
+                    constexpr int SLOTS = 6 / PL;                  // items a warp holds
+                    constexpr int CAP = 4 * SLOTS;                 // items a round stages
+                    static_assert(CAP * PL <= 4 * C::FIN_ITEMS, "staging rows");
+                    const int tr = nseg >= CAP ? 1 : min(4, CAP / nseg);
+                    const uint64_t* pb = reinterpret_cast<const uint64_t*>(p.part) + lane * 4;
+                    const size_t sw = (size_t)2 * B * 128;
+                    const uint32_t want = (uint32_t)(l + 1);
+                    float4* stg = fin_buf;             // the whole staging area, [item][plane][lane]
+                    for (int tb = t_lo; tb < t_hi; tb += tr) {
+                        const int ntr = min(tr, t_hi - tb);
+                        const int t = tb + q;                      // the token this warp adds up (q < ntr)
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+                        uint2 rv = make_uint2(0u, 0u);
+                        float ssq = 0.f;
+                        if (q < ntr) {
+                            if (has_resid && r0 < D) rv = __ldcg(reinterpret_cast<const uint2*>(resid + (int64_t)t * D + r0));
+                            if constexpr (NO) ssq = tile_sums(sl, Dt, B, t, lane);
+                        }
+                        const int step = ntr == 1 ? CAP : nseg;
+                        for (int c0 = 0; c0 < nseg; c0 += step) {
+                            const int cn = min(step, nseg - c0);
+                            const int nit = ntr * cn;
+                            ulonglong2 w[SLOTS][PL][2];
+                            auto item_ptr = [&](int i) {
+                                const int j = i / cn;
+                                return pb + (size_t)slot_of(c0 + (i - j * cn)) * sw + (size_t)(tb + j) * 128;
+                            };
+#pragma unroll
+                            for (int s2 = 0; s2 < SLOTS; ++s2) {
+                                const int i = q + 4 * s2;
+                                if (i < nit) {
+                                    const uint64_t* ip = item_ptr(i);
+#pragma unroll
+                                    for (int pl = 0; pl < PL; ++pl) {
+                                        w[s2][pl][0] = ld_tagged2(ip + (size_t)pl * B * 128);
+                                        w[s2][pl][1] = ld_tagged2(ip + (size_t)pl * B * 128 + 2);
+                                    }
+                                }
+                            }
+                            const uint64_t t_start = globaltimer();
+                            for (uint32_t it = 0;; ++it) {
+                                bool all = true;
+#pragma unroll
+                                for (int s2 = 0; s2 < SLOTS; ++s2) {
+                                    const int i = q + 4 * s2;
+                                    bool ok = true;
+#pragma unroll
+                                    for (int pl = 0; pl < PL; ++pl) {
+#pragma unroll
+                                        for (int h2 = 0; h2 < 2; ++h2)
+                                            ok = ok && (uint32_t)(w[s2][pl][h2].x >> 32) == want &&
+                                                 (uint32_t)(w[s2][pl][h2].y >> 32) == want;
+                                    }
+                                    if (i < nit && !ok) {
+                                        all = false;
+                                        const uint64_t* ip = item_ptr(i);
+#pragma unroll
+                                        for (int pl = 0; pl < PL; ++pl) {
+                                            w[s2][pl][0] = ld_tagged2(ip + (size_t)pl * B * 128);
+                                            w[s2][pl][1] = ld_tagged2(ip + (size_t)pl * B * 128 + 2);
+                                        }
+                                    }
+                                }
+                                if (__all_sync(0xFFFFFFFFu, all)) break;
+                                if ((it & 15u) == 15u &&
+                                    __any_sync(0xFFFFFFFFu, *labort || *gabort || globaltimer() - t_start > p.wait_ns)) {
+                                    if (lane == 0) fail();
+                                    break;
+                                }
+                            }
+#pragma unroll
+                            for (int s2 = 0; s2 < SLOTS; ++s2) {
+                                const int i = q + 4 * s2;
+                                if (i < nit) {
+#pragma unroll
+                                    for (int pl = 0; pl < PL; ++pl)
+                                        stg[(i * PL + pl) * 32 + lane] =
+                                            make_float4(__uint_as_float((uint32_t)w[s2][pl][0].x), __uint_as_float((uint32_t)w[s2][pl][0].y),
+                                                        __uint_as_float((uint32_t)w[s2][pl][1].x), __uint_as_float((uint32_t)w[s2][pl][1].y));
+                                }
+                            }
+                            epi_sync();
+                            if (q < ntr) {
+                                for (int k2 = 0; k2 < cn; ++k2) {
+                                    const int i = q * cn + k2;
+                                    add4(acc, stg[(i * PL) * 32 + lane]);
+                                    if constexpr (DU) add4(acc2, stg[(i * PL + 1) * 32 + lane]);
+                                }
+                            }
+                            epi_sync();
+                        }
+                        if (q < ntr) {
+                            float sc = 1.f;
+                            if constexpr (NO) sc = 1.0f / sqrtf(warp_sum32(ssq) / (float)D + p.eps);
+                            emit(t, acc, acc2, rv, sc);
+                        }
+                    }
+                };
                 using I1 = std::integral_constant<int, 1>;
                 using I2 = std::integral_constant<int, 2>;
                 auto share = [&](auto dual_c, auto norm_c) {
                     constexpr int PL = decltype(dual_c)::value ? 2 : 1;
                     // three tokens a batch at 128 columns, where a CTA finalizes ~60-200 pairs
-                    if (NP == 128 && 3 * PL * nseg <= C::FIN_ITEMS) {
-                        share_tb(std::integral_constant<int, 3>{}, dual_c, norm_c);
-                        return;
+                    if constexpr (NP == 128) {
+                        if (3 * PL * nseg <= C::FIN_ITEMS) {
+                            share_tb(std::integral_constant<int, 3>{}, dual_c, norm_c);
+                            return;
+                        }
                     }
-                    if (NP > 32 && 2 * PL * nseg <= C::FIN_ITEMS) share_tb(I2{}, dual_c, norm_c);
-                    else share_tb(I1{}, dual_c, norm_c);
+                    if constexpr (NP > 32) {
+                        if (2 * PL * nseg <= C::FIN_ITEMS) {
+                            share_tb(I2{}, dual_c, norm_c);
+                            return;
+                        }
+                    }
+                    share_tb(I1{}, dual_c, norm_c);
                 };
                 using T = std::true_type;
                 using Fa = std::false_type;
-                if (dual) share(T{}, T{});
-                else if (normed) share(Fa{}, T{});
-                else share(Fa{}, Fa{});
+                if constexpr (LL) {
+                    if (dual) share_ll(T{}, T{});
+                    else if (normed) share_ll(Fa{}, T{});
+                    else share_ll(Fa{}, Fa{});
+                } else {
+                    if (dual) share(T{}, T{});
+                    else if (normed) share(Fa{}, T{});
+                    else share(Fa{}, Fa{});
+                }
                 // this CTA's share of the tile is written: count it on the
                 // tile (the next phase's activation loads wait for that) and
                 // on the phase
                 epi_sync();
-                if (leader && !dead)
+                if (leader && !dead && !*labort)
                     publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)(t_hi - t_lo));
                 if (leader) TPL_TRACE(k, 5);
             }
@@ -1071,7 +1263,8 @@ void segment_caps(const FusedShape& sh, int G, int (&cap)[4]) {
 }
 
 // Test hook state (set by tpl_test_fused_fault): the next launches' wait
-// limit and the CTA / phase whose first ticket arrival is left out.
+// limit and the CTA / phase whose first unit is not delivered (no ticket,
+// or no tagged words).
 std::atomic<int> g_skip_cta{-1}, g_skip_phase{-1};
 std::atomic<long long> g_wait_ns{0};
 
@@ -1110,6 +1303,10 @@ FusedPlan plan_fused(const FusedShape& s) {
     f.tick_off = o; o += up256((size_t)4 * f.max_mt * 4);
     f.ready_off = o; o += up256((size_t)4 * f.max_mt * 4);
     f.done_off = o; o += up256((size_t)(1 + 4 * kFusedMaxLayers) * 4);
+    // narrow instantiations: tagged partial words [4 kinds][slots][2][B][128] u64, zeroed
+    // with the counters before each launch (a stale word never carries a live tag)
+    const bool tagged = f.np <= kTaggedNP;
+    if (tagged) { f.part_off = o; o += up256((size_t)4 * (kFusedGridCap + f.max_mt) * 2 * s.B * 128 * 8); }
     f.sy_off = o; o += up256((size_t)Dt * s.B * 4);
     f.sh_off = o; o += up256((size_t)Dt * s.B * 4);
     f.r0_off = o; o += up256((size_t)s.B * s.D * 2);
@@ -1118,7 +1315,7 @@ FusedPlan plan_fused(const FusedShape& s) {
     f.hid_off = o; o += up256((size_t)s.B * s.F * 2);
     f.qkv_off = o; o += up256((size_t)s.tp * s.B * w_s * 2);
     // one region of partial slots per projection kind
-    f.part_off = o; o += up256((size_t)4 * (kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4);
+    if (!tagged) { f.part_off = o; o += up256((size_t)4 * (kFusedGridCap + f.max_mt) * 2 * f.np * 128 * 4); }
     f.total = o;
     return f;
 }
