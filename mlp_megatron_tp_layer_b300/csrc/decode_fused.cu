@@ -153,7 +153,7 @@ struct Phase {
     int prev_fin;              // phase whose completion this phase's finalize waits for (-1: none)
     int src_kind;              // kind whose output tiles the activation loads wait for (-1: launch input)
     unsigned src_target;       // ready count of such a tile once this layer's input is final
-    int64_t total;
+    int total;                 // m_tiles x nkb (the shape check keeps total x G below 2^31)
     const CUtensorMap* wa;
     const CUtensorMap* wb;
     const CUtensorMap* act;
@@ -207,7 +207,7 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     ph.wb = wb < 0 ? nullptr : &mp.w[l][wb];
     ph.m_tiles = (ph.M + 127) / 128;
     ph.nkb = (K + 63) / 64;
-    ph.total = (int64_t)ph.m_tiles * ph.nkb;
+    ph.total = ph.m_tiles * ph.nkb;
     // every tile split into exactly s segments when m_tiles x s CTAs still
     // cover at least 94% of the grid (fewer, aligned segments: less partial
     // traffic per tile; the CTAs left over stream no weights in this phase)
@@ -270,39 +270,41 @@ __device__ __forceinline__ int src_tile(const FusedParams& p, const Phase& ph, i
 }
 
 // The CTA owning flattened index a: the largest c with floor(c T / G) <= a.
-__device__ __forceinline__ int owner_of(int64_t a, int64_t total, int G) {
-    return (int)(((a + 1) * G - 1) / total);
+__device__ __forceinline__ int owner_of(int a, int total, int G) {
+    return (int)((unsigned)((a + 1) * G - 1) / (unsigned)total);
 }
 
 // Whether CTA c's range is non-empty (always, unless the phase has fewer
 // (m-tile, k-block) pairs than CTAs).
-__device__ __forceinline__ bool has_work(int64_t total, int G, int c) {
-    return total * (c + 1) / G > total * c / G;
+__device__ __forceinline__ bool has_work(int total, int G, int c) {
+    return (unsigned)(total * (c + 1)) / (unsigned)G > (unsigned)(total * c) / (unsigned)G;
 }
 
 // The split part of a phase: the flattened (m-tile, k-block) pairs from
 // index seg_base on (the tiles after the whole ones), seg_total of them,
 // split over CTAs 0 .. gw-1.
-__device__ __forceinline__ int64_t seg_base(const Phase& ph) { return (int64_t)ph.whole * ph.nkb; }
-__device__ __forceinline__ int64_t seg_total(const Phase& ph) { return ph.total - seg_base(ph); }
+__device__ __forceinline__ int seg_base(const Phase& ph) { return ph.whole * ph.nkb; }
+__device__ __forceinline__ int seg_total(const Phase& ph) { return ph.total - seg_base(ph); }
 
 // The units (m-tile, k-block range) of CTA c in a phase, in k order: its
 // whole tile if it has one (WH), then its range [idx2, hi2) of the split part.
 template <bool WH>
 struct Units {
-    int64_t idx, hi, idx2, hi2;
+    int idx, hi, idx2, hi2;
     int nkb;
     __device__ __forceinline__ Units() : idx(0), hi(0), idx2(0), hi2(0), nkb(1) {}
     __device__ __forceinline__ Units(const Phase& ph, int c) : nkb(ph.nkb) {
+        const unsigned gw = (unsigned)ph.gw;
         if constexpr (WH) {
-            const int64_t b = seg_base(ph), t = seg_total(ph);
-            idx = c < ph.whole ? (int64_t)c * ph.nkb : 0;
+            const int b = seg_base(ph);
+            const unsigned t = (unsigned)seg_total(ph);
+            idx = c < ph.whole ? c * ph.nkb : 0;
             hi = c < ph.whole ? idx + ph.nkb : 0;
-            idx2 = c < ph.gw ? b + t * c / ph.gw : 0;
-            hi2 = c < ph.gw ? b + t * (c + 1) / ph.gw : 0;
+            idx2 = c < ph.gw ? b + (int)(t * c / gw) : 0;
+            hi2 = c < ph.gw ? b + (int)(t * (c + 1) / gw) : 0;
         } else {
-            idx = c < ph.gw ? ph.total * c / ph.gw : 0;
-            hi = c < ph.gw ? ph.total * (c + 1) / ph.gw : 0;
+            idx = c < ph.gw ? (int)((unsigned)ph.total * c / gw) : 0;
+            hi = c < ph.gw ? (int)((unsigned)ph.total * (c + 1) / gw) : 0;
             idx2 = hi2 = 0;
         }
     }
@@ -313,9 +315,9 @@ struct Units {
             hi = hi2;
             idx2 = hi2 = 0;
         }
-        mt = (int)(idx / nkb);
-        kb0 = (int)(idx - (int64_t)mt * nkb);
-        kb1 = (int)min((int64_t)nkb, (int64_t)kb0 + (hi - idx));
+        mt = (int)((unsigned)idx / (unsigned)nkb);
+        kb0 = idx - mt * nkb;
+        kb1 = min(nkb, kb0 + (hi - idx));
         idx += kb1 - kb0;
         return true;
     }
@@ -462,12 +464,12 @@ __device__ __forceinline__ void publish2(unsigned* a, unsigned* b, unsigned v) {
 // same in every lane; 0: the wait gave up (time limit or abort).  Every lane
 // then fences the async proxy, so the TMA loads issued after the warp
 // barrier see the tiles' contents.
-__device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& ph, int64_t idx, int64_t hi,
+__device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& ph, int idx, int hi,
                                             int lane, volatile int* labort, volatile int* gabort) {
-    const int want = (int)min(hi - idx, (int64_t)32);
+    const int want = min(hi - idx, 32);
     const unsigned* ctr = nullptr;
     if (lane < want) {
-        const int kb = (int)((idx + lane) % ph.nkb);
+        const int kb = (int)((unsigned)(idx + lane) % (unsigned)ph.nkb);
         ctr = p.ready + ph.src_kind * p.max_mt + src_tile(p, ph, kb);
     }
     const uint64_t t0 = globaltimer();
@@ -605,9 +607,9 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const int halves = ph.kind == K_GATEUP ? 2 : 1;
             const Units<WH> u(ph, cta);        // this CTA's pairs: [u.idx, u.hi) then [u.idx2, u.hi2)
             for (int range = 0; range < (WH ? 2 : 1) && ok; ++range) {
-                const int64_t r_lo = range ? u.idx2 : u.idx, r_hi = range ? u.hi2 : u.hi;
-                for (int64_t idx = r_lo; ok && idx < r_hi;) {
-                    int n = (int)min(r_hi - idx, (int64_t)32);
+                const int r_lo = range ? u.idx2 : u.idx, r_hi = range ? u.hi2 : u.hi;
+                for (int idx = r_lo; ok && idx < r_hi;) {
+                    int n = min(r_hi - idx, 32);
                     const bool first_k = idx == (u.idx < u.hi ? u.idx : u.idx2);
                     if (first_k && lane == 0) TPL_TRACE(k, 7);
                     if (ph.src_kind >= 0) {
@@ -616,8 +618,8 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     }
                     if (first_k && lane == 0) TPL_TRACE(k, 0);
                     if (lane == 0) {
-                        for (int j = 0; j < n && ok; ++j) {
-                            const int kb = (int)((idx + j) % ph.nkb);
+                        int kb = (int)((unsigned)idx % (unsigned)ph.nkb);
+                        for (int j = 0; j < n && ok; ++j, kb = kb + 1 == ph.nkb ? 0 : kb + 1) {
                             for (int hf = 0; hf < halves; ++hf) {
                                 if (!mbar_wait(smem_addr(&empty[stage]), par ^ 1, labort, gabort, p.wait_ns)) { ok = false; break; }
                                 const uint32_t fb = smem_addr(&full_x[stage]);
@@ -900,10 +902,10 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             // which hold work unless the phase has fewer pairs than CTAs (then
             // warp 2 lists the ones that do into list / seg_info[info])
             auto seg_list = [&](const Phase& phx, int mt_, int* list, int info, int& cf_, bool& every_) {
-                const int64_t sb = seg_base(phx), st = seg_total(phx);
+                const int sb = seg_base(phx), st = seg_total(phx);
                 every_ = st >= phx.gw;
-                cf_ = owner_of((int64_t)mt_ * phx.nkb - sb, st, phx.gw);
-                const int cl_ = owner_of((int64_t)mt_ * phx.nkb + phx.nkb - 1 - sb, st, phx.gw);
+                cf_ = owner_of(mt_ * phx.nkb - sb, st, phx.gw);
+                const int cl_ = owner_of(mt_ * phx.nkb + phx.nkb - 1 - sb, st, phx.gw);
                 if (!every_ && warp == 2) {
                     int n = 0;
                     for (int base = cf_; base <= cl_; base += 32) {
@@ -921,14 +923,14 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
             bool prev_done = ph.prev_fin < 0;
             // (tiles before ph.whole were finished whole in pass 1)
-            const int64_t npairs = (int64_t)(ph.m_tiles - ph.whole) * B;
-            const int64_t f1 = npairs * (cta + 1) / G;
-            for (int64_t f = npairs * cta / G; f < f1;) {
-                const int64_t fm = f / B;               // tile index among the split tiles
+            const unsigned npairs = (unsigned)((ph.m_tiles - ph.whole) * B);
+            const int f1 = (int)(npairs * (cta + 1) / (unsigned)G);
+            for (int f = (int)(npairs * cta / (unsigned)G); f < f1;) {
+                const int fm = (int)((unsigned)f / (unsigned)B);   // tile index among the split tiles
                 mt = ph.whole + (int)fm;
                 // this CTA's tokens of tile mt
                 const int t_lo = (int)(f - fm * B);
-                const int t_hi = (int)min((int64_t)B, f1 - fm * B);
+                const int t_hi = min(B, f1 - fm * B);
                 f = fm * B + t_hi;
                 int cf, cf_o = 0;
                 bool every, every_o = true;
@@ -1110,7 +1112,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                             const int nit = ntr * cn;
                             ulonglong2 w[SLOTS][PL][2];
                             auto item_ptr = [&](int i) {
-                                const int j = i / cn;
+                                const int j = (int)((unsigned)i / (unsigned)cn);
                                 return pb + (size_t)slot_of(c0 + (i - j * cn)) * sw + (size_t)(tb + j) * 128;
                             };
 #pragma unroll
@@ -1357,7 +1359,13 @@ void fused_test_fault(int cta, int phase, long long wait_ns) {
 bool fused_stack_shape_ok(const FusedShape& s) {
     if (s.B < 1 || s.B > 128) return false;
     if (s.D % 64 || s.F % 64 || s.hd % 64) return false;
-    return s.D <= (1 << 20) && s.F <= (1 << 20) && (int64_t)(s.n_q + 2 * s.n_kv) * s.hd <= (1 << 20);
+    const int64_t n_qkv = (int64_t)(s.n_q + 2 * s.n_kv) * s.hd, ko = (int64_t)s.n_q * s.hd;
+    if (s.D > (1 << 20) || s.F > (1 << 20) || n_qkv > (1 << 20)) return false;
+    // the work split indexes (m-tile, k-block) pairs in 32 bits: pairs x G < 2^31
+    const int64_t MK[4][2] = {{n_qkv, s.D}, {s.D, ko}, {s.F, s.D}, {s.D, s.F}};
+    for (const auto& mk : MK)
+        if ((mk[0] + 127) / 128 * (mk[1] / 64) * kFusedGridCap >= (int64_t(1) << 31)) return false;
+    return true;
 }
 
 size_t fused_stack_ws_bytes(const FusedShape& s) { return plan_fused(s).total; }
