@@ -595,7 +595,8 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
         // issues the copies).  The second stage of a gate/up k-block reuses the
         // first one's activations: its activation barrier still completes a
         // phase (a plain arrive), so every barrier of the ring advances once
-        // per round and the parities stay in step.
+        // per round, and the MMA issuer waits for that arrive too, so no
+        // producer falls a round behind the releases it waits for.
         const uint64_t pol = policy_evict_last();
         int stage = 0;
         uint32_t par = 0;
@@ -685,7 +686,12 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                         uint32_t p2 = par;
                         if (s2 == C::STAGES) { s2 = 0; p2 ^= 1; }
                         if (dual) {
-                            if (!mbar_wait(smem_addr(&full_w[s2]), p2, labort, gabort, p.wait_ns)) { ok = false; break; }
+                            // the up half's stage: its weights, and the activation
+                            // producer's plain arrive (waited for so that the MMA
+                            // never releases the stage a round before the producer
+                            // has waited for it: the parity waits would alias)
+                            if (!mbar_wait(smem_addr(&full_w[s2]), p2, labort, gabort, p.wait_ns) ||
+                                !mbar_wait(smem_addr(&full_x[s2]), p2, labort, gabort, p.wait_ns)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t sw2 = smem_addr(smem + s2 * C::STAGE);
 #pragma unroll
