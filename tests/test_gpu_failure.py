@@ -107,3 +107,32 @@ def test_phase_trace_is_only_in_the_instrumented_build():
         assert st == 0
     else:
         assert tpl.STATUS[st] == "TPL_ERR_UNSUPPORTED"
+
+
+# Repeated launches at the shapes where every k-block's activations arrive fast
+# (small batches): a ring whose barrier phases could alias two rounds apart
+# (a producer waiting for a release the consumer has already given twice)
+# hangs only when a race is lost, so one launch proves little.  Every launch
+# must end cleanly with the same bits.
+@pytest.mark.parametrize("model,block,B,L,reps", [
+    ("qwen", tpl.BLOCK_PARALLEL, 8, 28, 60),
+    ("qwen", tpl.BLOCK_SERIAL, 1, 28, 60),
+    ("llama", tpl.BLOCK_SERIAL, 1, 2, 30),
+])
+def test_fused_stack_repeated_launches_stay_clean(model, block, B, L, reps):
+    cfg = si.QWEN_DECODE if model == "qwen" else si.LLAMA_DECODE
+    D, F, n_q, n_kv, hd, tp = cfg["D"], cfg["F"], cfg["n_q"], cfg["n_kv"], cfg["head_dim"], cfg["tp"]
+    layers = [si.layer_weights(D, F, n_q, n_kv, hd, seed=0, layer=l, prefix=model, device="cuda")
+              for l in range(L)]
+    x = si.activations(B, D, seed=5, name=f"{model}.rep{B}", device="cuda")
+    ws = tpl.workspace(tpl.decoder_workspace_bytes(B, D, F, n_q, n_kv, hd, tp), "cuda")
+    tpl.test_fused_fault(-1, 1, 200_000_000)           # a lost race ends in 0.2 s, not 2 s
+    ref = None
+    for r in range(reps):
+        y = tpl.tp_decoder_stack(x, layers, n_q, n_kv, hd, tp, ws=ws, path=tpl.PATH_FUSED, block=block)
+        torch.cuda.synchronize()
+        assert tpl.device_status() == 0, f"launch {r} timed out"
+        if ref is None:
+            ref = y.clone()
+        else:
+            assert torch.equal(y, ref), f"launch {r} differs from the first"
