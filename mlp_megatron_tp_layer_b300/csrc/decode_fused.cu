@@ -150,6 +150,7 @@ struct Phase {
     int kind, layer, m_tiles, nkb, M;
     int gw;                    // CTAs holding units of the phase: 0 .. gw-1
     int whole;                 // tiles 0 .. whole-1 go whole to CTAs 0 .. whole-1 (0: none)
+    int rev;                   // 1: a CTA takes its units last tile first (see phase_of)
     int prev_fin;              // phase whose completion this phase's finalize waits for (-1: none)
     int src_kind;              // kind whose output tiles the activation loads wait for (-1: launch input)
     unsigned src_target;       // ready count of such a tile once this layer's input is final
@@ -218,6 +219,11 @@ __device__ __forceinline__ Phase phase_of(const FusedMaps& mp, const FusedParams
     // (only the 128-column instantiation carries this path: it pays at 65-128
     // tokens, where the gate/up finalize is long)
     ph.whole = (WH && ph.kind == K_GATEUP && ph.m_tiles >= p.G) ? p.G : 0;
+    // down after whole gate/up tiles: H tiles 0 .. G-1 are final long before
+    // the split ones, so a CTA whose range starts among the split tiles' k-blocks
+    // and runs into the next m-tile takes that next tile's unit first (units
+    // are separate partials: their order changes no sum)
+    ph.rev = (WH && ph.kind == K_DOWN && (p.F + 127) / 128 >= p.G) ? 1 : 0;
     if (ph.whole) return ph;
     const int s = min(p.G / ph.m_tiles, ph.nkb);
     if (s > p.s_cap[ph.kind]) ph.gw = ph.m_tiles * p.s_cap[ph.kind];
@@ -292,8 +298,9 @@ template <bool WH>
 struct Units {
     int idx, hi, idx2, hi2;
     int nkb;
-    __device__ __forceinline__ Units() : idx(0), hi(0), idx2(0), hi2(0), nkb(1) {}
-    __device__ __forceinline__ Units(const Phase& ph, int c) : nkb(ph.nkb) {
+    bool rev;
+    __device__ __forceinline__ Units() : idx(0), hi(0), idx2(0), hi2(0), nkb(1), rev(false) {}
+    __device__ __forceinline__ Units(const Phase& ph, int c) : nkb(ph.nkb), rev(WH && ph.rev) {
         const unsigned gw = (unsigned)ph.gw;
         if constexpr (WH) {
             const int b = seg_base(ph);
@@ -314,6 +321,14 @@ struct Units {
             idx = idx2;
             hi = hi2;
             idx2 = hi2 = 0;
+        }
+        if (WH && rev) {                    // the range's last m-tile first
+            mt = (int)((unsigned)(hi - 1) / (unsigned)nkb);
+            const int start = max(idx, mt * nkb);
+            kb0 = start - mt * nkb;
+            kb1 = hi - mt * nkb;
+            hi = start;
+            return true;
         }
         mt = (int)((unsigned)idx / (unsigned)nkb);
         kb0 = idx - mt * nkb;
@@ -607,11 +622,12 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const Phase ph = phase_of<WH>(mp, p, k);
             const int halves = ph.kind == K_GATEUP ? 2 : 1;
             const Units<WH> u(ph, cta);        // this CTA's pairs: [u.idx, u.hi) then [u.idx2, u.hi2)
-            for (int range = 0; range < (WH ? 2 : 1) && ok; ++range) {
-                const int r_lo = range ? u.idx2 : u.idx, r_hi = range ? u.hi2 : u.hi;
+            // the pairs [r_lo, r_hi) in order: ready polls of up to 32 at a time,
+            // then one copy per k-block
+            auto feed = [&](int r_lo, int r_hi, bool first_range) {
                 for (int idx = r_lo; ok && idx < r_hi;) {
                     int n = min(r_hi - idx, 32);
-                    const bool first_k = idx == (u.idx < u.hi ? u.idx : u.idx2);
+                    const bool first_k = first_range && idx == r_lo;
                     if (first_k && lane == 0) TPL_TRACE(k, 7);
                     if (ph.src_kind >= 0) {
                         n = ready_prefix(p, ph, idx, r_hi, lane, labort, gabort);
@@ -641,6 +657,19 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
                     idx += n;
                 }
+            };
+            if (WH && ph.rev) {
+                // unit by unit, in the order the MMA issuer takes them
+                Units<WH> uu(ph, cta);
+                int mt_u, kb0_u, kb1_u;
+                bool first_u = true;
+                while (ok && uu.next(mt_u, kb0_u, kb1_u)) {
+                    feed(mt_u * ph.nkb + kb0_u, mt_u * ph.nkb + kb1_u, first_u);
+                    first_u = false;
+                }
+            } else {
+                for (int range = 0; range < (WH ? 2 : 1) && ok; ++range)
+                    feed(range ? u.idx2 : u.idx, range ? u.hi2 : u.hi, range == 0 ? u.idx < u.hi : u.idx >= u.hi);
             }
         }
         if (!ok && lane == 0) {
