@@ -52,6 +52,10 @@ struct TcParams {
     int64_t main_tiles;
     int tail_s;
     float* tail_ws;
+    // normal orientation with few m-tiles: A (tokens, reused by every n-tile)
+    // is loaded evict_last and B (weights, read by the few CTAs of one wave)
+    // evict_first, so the streamed weights do not push A out of L2
+    int hint_ab;
 };
 
 template <int BN, bool SWAP, bool DUAL>
@@ -192,6 +196,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         tma_load_hint(smem_addr(st), &tmA, fb, kx, am, pol_w);
                         if (DUAL) tma_load_hint(smem_addr(st + C::A_BYTES), &tmA2, fb, kx, am, pol_w);
                         tma_load_hint(smem_addr(st + C::A_BYTES + C::A2_BYTES), &tmB, fb, kx, bn, pol_x);
+                    } else if (p.hint_ab) {
+                        tma_load_hint(smem_addr(st), &tmA, fb, kx, am, pol_x);
+                        tma_load_hint(smem_addr(st + C::A_BYTES), &tmB, fb, kx, bn, pol_w);
+                        if (DUAL) tma_load_hint(smem_addr(st + C::A_BYTES + C::B_BYTES / 2), &tmB2, fb, kx, bn, pol_w);
                     } else {
                         tma_load(smem_addr(st), &tmA, fb, kx, am);
                         tma_load(smem_addr(st + C::A_BYTES), &tmB, fb, kx, bn);
@@ -444,6 +452,10 @@ cudaError_t launch_cfg(const TcGemmArgs& a, cudaStream_t st) {
     p.main_tiles = p.total_tiles;
     p.tail_s = 0;
     p.tail_ws = nullptr;
+    // (measured: the sharded-matmul cases, 4 m-tiles, 834-839 -> 864-866 TFLOP/s;
+    // the 4096-token prefill, 32 m-tiles, is slower with it: its weights are
+    // read by 32 CTAs and evict_first loses them between readers)
+    p.hint_ab = (!SWAP && p.m_tiles <= 8) ? 1 : 0;
     if (!SWAP && !DUAL && C::OUT_COLS == 256 && a.epi.mode == EPI_STORE && p.splits == 1 && a.tail_ws) {
         const TailPlan t = tail_plan(a.M, a.N, a.K, ctx->num_sms);
         if (t.s > 0 && t.bytes <= a.tail_ws_bytes) {
