@@ -958,9 +958,20 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
             const bool normed = ph.kind == K_QKV || ph.kind == K_GATEUP;
             bool prev_done = ph.prev_fin < 0;
             // (tiles before ph.whole were finished whole in pass 1)
-            const unsigned npairs = (unsigned)((ph.m_tiles - ph.whole) * B);
-            const int f1 = (int)(npairs * (cta + 1) / (unsigned)G);
-            for (int f = (int)(npairs * cta / (unsigned)G); f < f1;) {
+            // 128 columns, QKV: the tiles holding V rows first, spread over every
+            // CTA, then the Q and K tiles.  o_proj reads only V, so its stream
+            // starts while the rest is being finalized (which CTA adds which
+            // pair changes no sum).  (Measured: +2% on the Llama-3.1-70B shape at
+            // 128 tokens, where a CTA finalizes ~70 pairs; at a few pairs a CTA
+            // it moved V's finalizers away from V's segments and cost up to 7%.)
+            const int nsplit = ph.m_tiles - ph.whole;
+            const int pt0 = (NP == 128 && ph.kind == K_QKV)
+                ? min(nsplit, (p.qkv.n_q + p.qkv.n_kv) * p.qkv.head_dim / 128) : nsplit;
+            for (int rg = 0; rg < 2; ++rg) {
+            const unsigned npairs = (unsigned)((rg == 0 ? nsplit - pt0 : pt0) * B);
+            const int fbase = rg == 0 ? pt0 * B : 0;
+            const int f1 = fbase + (int)(npairs * (cta + 1) / (unsigned)G);
+            for (int f = fbase + (int)(npairs * cta / (unsigned)G); f < f1;) {
                 const int fm = (int)((unsigned)f / (unsigned)B);   // tile index among the split tiles
                 mt = ph.whole + (int)fm;
                 // this CTA's tokens of tile mt
@@ -1258,6 +1269,7 @@ fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
                 if (leader && !dead && !*labort)
                     publish2(p.ready + ph.kind * p.max_mt + mt, p.done + k, (unsigned)(t_hi - t_lo));
                 if (leader) TPL_TRACE(k, 5);
+            }
             }
         }
     }
