@@ -511,11 +511,15 @@ __device__ __forceinline__ int ready_prefix(const FusedParams& p, const Phase& p
     }
 }
 
-template <int NP>
+template <int NP, bool WHT>
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_stack_kernel(const __grid_constant__ FusedMaps mp, const FusedParams p) {
     using C = FCfg<NP>;
-    constexpr bool WH = NP == 128;       // gate/up tiles taken whole when there are at least G of them
+    // gate/up tiles taken whole (the launch picks this build when gate/up has
+    // at least one 128-row tile per CTA: at 32 and 128 columns, where the
+    // gate/up finalize is long; built without it, the other shapes skip its
+    // extra unit ranges, which cost them about 1%)
+    constexpr bool WH = WHT;
     constexpr bool LL = NP <= kTaggedNP;  // tagged partial words instead of tile tickets
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1369,7 +1373,16 @@ FusedPlan plan_fused(const FusedShape& s) {
     return f;
 }
 
-template <int NP>
+// Shared-memory limit of one build, and how many of its CTAs fit an SM.
+template <int NP, bool WHT>
+cudaError_t prep_np(int smem, int& per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(fused_stack_kernel<NP, WHT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<NP, WHT>, kFThreads, smem);
+    return e;
+}
+
+template <int NP, bool WHT>
 cudaError_t launch_np(const FusedMaps& maps, const FusedParams& prm, cudaStream_t st) {
     using C = FCfg<NP>;
     cudaLaunchConfig_t cfg = {};
@@ -1382,7 +1395,7 @@ cudaError_t launch_np(const FusedMaps& maps, const FusedParams& prm, cudaStream_
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_stack_kernel<NP>, maps, prm);
+    return cudaLaunchKernelEx(&cfg, fused_stack_kernel<NP, WHT>, maps, prm);
 }
 
 }  // namespace
@@ -1428,23 +1441,27 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
     const int64_t ko = (int64_t)s.n_q * s.hd;
 
     int G = std::min(ctx->num_sms, kFusedGridCap);
+    bool wh = false;       // the build with whole gate/up tiles
     {
         int per_sm = 0;
         const int smem = smem_for(f.np);
         cudaError_t e = cudaSuccess;
         switch (f.np) {
-        case 16: e = cudaFuncSetAttribute(fused_stack_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<16>, kFThreads, smem); break;
-        case 32: e = cudaFuncSetAttribute(fused_stack_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<32>, kFThreads, smem); break;
-        case 64: e = cudaFuncSetAttribute(fused_stack_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<64>, kFThreads, smem); break;
-        default: e = cudaFuncSetAttribute(fused_stack_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                 if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_stack_kernel<128>, kFThreads, smem); break;
+        case 16: e = prep_np<16, false>(smem, per_sm); break;
+        case 32: e = prep_np<32, false>(smem, per_sm); break;
+        case 64: e = prep_np<64, false>(smem, per_sm); break;
+        default: e = prep_np<128, false>(smem, per_sm); break;
         }
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         G = std::min(G, per_sm * ctx->num_sms);
+        wh = (f.np == 32 || f.np == 128) && (s.F + 127) / 128 >= G;
+        if (wh) {
+            int per_sm_wh = 0;
+            e = f.np == 32 ? prep_np<32, true>(smem, per_sm_wh) : prep_np<128, true>(smem, per_sm_wh);
+            if (e != cudaSuccess) return e;
+            if (per_sm_wh < per_sm) return cudaErrorInvalidConfiguration;
+        }
     }
 
     FusedParams prm{};
@@ -1505,10 +1522,10 @@ cudaError_t launch_fused_stack(const FusedShape& s, const void* x, void* y, cons
         cudaError_t e = cudaMemsetAsync(w + f.ctrl_off, 0, f.sy_off - f.ctrl_off, st);
         if (e != cudaSuccess) return e;
         switch (np) {
-        case 16: e = launch_np<16>(maps, prm, st); break;
-        case 32: e = launch_np<32>(maps, prm, st); break;
-        case 64: e = launch_np<64>(maps, prm, st); break;
-        default: e = launch_np<128>(maps, prm, st); break;
+        case 16: e = launch_np<16, false>(maps, prm, st); break;
+        case 32: e = wh ? launch_np<32, true>(maps, prm, st) : launch_np<32, false>(maps, prm, st); break;
+        case 64: e = launch_np<64, false>(maps, prm, st); break;
+        default: e = wh ? launch_np<128, true>(maps, prm, st) : launch_np<128, false>(maps, prm, st); break;
         }
         if (e != cudaSuccess) return e;
     }
