@@ -557,9 +557,7 @@ def run_llama_decode(args, tpl, dev, world, peaks, peak_kind, stream):
            "per_batch": {}}
     reps = max(3, args.steps // 4)
     for B in batches:
-        for _ in range(2):
-            graphs[B].replay()
-        torch.cuda.synchronize()
+        warm_up(graphs[B].replay, n_min=2)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(reps):
@@ -623,9 +621,7 @@ def run_lm_head(args, tpl, dev, peaks, stream, k=1):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 tpl.vocab_parallel_topk(x, W, tp, k, out=(idx, val), ws=ws)
-            for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize()
+            warm_up(g.replay)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             for _ in range(reps):
@@ -697,9 +693,7 @@ def run_w8_mlp(args, tpl, dev, peaks, stream):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     call()
-                for _ in range(3):
-                    g.replay()
-                torch.cuda.synchronize()
+                warm_up(g.replay)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 for _ in range(reps):
@@ -719,11 +713,22 @@ def run_w8_mlp(args, tpl, dev, peaks, stream):
     return out
 
 
-def time_ms(fn, reps):
-    """Average device time of fn over reps calls (CUDA events, after 3 warm-up calls)."""
-    for _ in range(3):
+def warm_up(fn, min_ms=10.0, n_min=3):
+    """Untimed calls of fn: at least n_min of them and at least min_ms of wall
+    time.  Three calls alone left the first batch size timed after new weights
+    were created about 6 us slow on an 85 us lm_head call."""
+    for _ in range(n_min):
         fn()
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    while (time.perf_counter() - t0) * 1e3 < min_ms:
+        fn()
+        torch.cuda.synchronize()
+
+
+def time_ms(fn, reps):
+    """Average device time of fn over reps calls (CUDA events, after warm_up)."""
+    warm_up(fn)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(reps):

@@ -22,7 +22,10 @@
 // Kernel 2 (vocab_topk_merge_kernel): one block per (token, shard) reduces
 // that shard's tile candidates to the shard's top-k (the list a device would
 // send); the last block of each token to finish (an atomic ticket, no
-// waiting) merges the tp shard lists into the final top-k.
+// waiting) merges the tp shard lists into the final top-k.  It is launched as
+// a programmatic dependent of kernel 1, so its launch overlaps the GEMM's
+// last tiles; its blocks wait (griddepcontrol.wait) for the GEMM grid to
+// complete before reading any candidate.
 //
 // Candidate word: (order key of the fp32 logit) << 32 | (0xFFFFFFFF - index).
 // Comparing words as unsigned integers orders by logit, larger first, and
@@ -227,6 +230,8 @@ vocab_topk_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the merge kernel may be scheduled now; it waits for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -401,6 +406,8 @@ vocab_topk_merge_kernel(const unsigned long long* __restrict__ cand, unsigned lo
     __shared__ int s_last;
     const int64_t b = blockIdx.x;
     const int s = blockIdx.y;
+    // launched early behind the GEMM: wait until it has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // this shard's top-k for token b: the "local maximum / top-k" of one device
     unsigned long long L[kVocabTopkMax];
@@ -509,9 +516,21 @@ cudaError_t launch_vocab_topk(const VocabTopkArgs& a, cudaStream_t st) {
     else if (a.B <= 64) e = launch_bn<64>(a, p, st);
     else e = launch_bn<128>(a, p, st);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)a.B, (unsigned)a.tp);
-    vocab_topk_merge_kernel<<<grid, VT_MERGE_THREADS, 0, st>>>(cand, shard_best, tickets, a.B, a.tp, (int)tps, a.k,
-                                                               a.top_idx, a.top_val, a.shard_idx, a.shard_val);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)a.B, (unsigned)a.tp);
+    cfg.blockDim = dim3(VT_MERGE_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int tp_i = a.tp, tps_i = (int)tps, k_i = a.k;
+    const int64_t B_i = a.B;
+    e = cudaLaunchKernelEx(&cfg, vocab_topk_merge_kernel, (const unsigned long long*)cand, shard_best, tickets, B_i,
+                           tp_i, tps_i, k_i, a.top_idx, a.top_val, a.shard_idx, a.shard_val);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
