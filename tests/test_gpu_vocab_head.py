@@ -131,6 +131,33 @@ def test_vocab_topk_is_deterministic_and_fills_given_outputs():
     assert torch.equal(c[0], a[0]) and torch.equal(c[1], a[1])
 
 
+def test_vocab_topk_graph_replays_rank_each_replays_inputs():
+    """Captured in a CUDA graph, where the merge kernel is a programmatic
+    dependent of the GEMM: every replay ranks the inputs written before it,
+    exactly as an eager call on them does (a merge that read the candidates
+    before the GEMM completed would return the previous replay's answer)."""
+    B, D, V, tp, k = 5, 512, 6000, 2, 3
+    x, W = si.lm_head(B, D, V, seed=11, device="cuda")
+    fresh = [si.lm_head(B, D, V, seed=20 + i, device="cuda")[0] for i in range(3)]
+    idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    val = torch.empty(B, k, dtype=torch.float32, device="cuda")
+    ws = tpl.workspace(tpl.vocab_topk_workspace_bytes(B, V, tp, k), torch.device("cuda"))
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        tpl.vocab_parallel_topk(x, W, tp, k, out=(idx, val), ws=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        tpl.vocab_parallel_topk(x, W, tp, k, out=(idx, val), ws=ws)
+    for xn in fresh:
+        x.copy_(xn)
+        g.replay()
+        torch.cuda.synchronize()
+        want_idx, want_val = tpl.vocab_parallel_topk(xn, W, tp, k)
+        assert torch.equal(idx, want_idx) and torch.equal(val, want_val)
+    del g
+
+
 def test_exact_ties_resolve_to_the_lower_index_across_tiles_and_shards():
     B, D, V, tp = 3, 256, 4096, 4
     x, W = si.lm_head(B, D, V, seed=7, device="cuda")
